@@ -1,0 +1,327 @@
+"""Benchmark: fork decode attention on one B300 (or N, one independent problem per GPU).
+
+Metric: unique-KV HBM GB/s (the fraction of HBM peak is in ``roofline``) and branch-queries/s.
+One step = one fork_attn_decode (plan-driven kernels + merge) over the whole workload, inputs
+resident in HBM, L2 flushed (a 256 MiB write) between timed steps.  Default workload: the
+128K-token shared prefix with rolling tool drops, 64 branches (Hq 64 / Hkv 8).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1..5] [--impl ours|reference]
+
+Under torchrun every rank runs its own problem (seed offset by rank) on its GPU; rank 0 prints
+one JSON line.  ``--impl reference`` times the fp64 CPU oracle on bounded samples instead.
+"""
+import argparse
+import json
+import math
+import os
+import statistics
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import shared_prefix_paged_attn_b300 as fa  # noqa: E402
+from shared_prefix_paged_attn_b300 import workloads as W  # noqa: E402
+
+METRIC = "fork decode attention: unique-KV HBM GB/s (% of peak), branch-queries/sec"
+KV_BYTES_PER_SLOT_HEAD = 2 * 128 * 2  # K + V, bf16
+FALLBACK_HBM_GBS = 6400.0
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """Samples SM clock and throttle reasons through NVML while the timed region runs."""
+
+    def __init__(self, index, period_s=0.02):
+        self.index, self.period = index, period_s
+        self.samples, self.reasons = [], set()
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self._thr = None
+
+    def __enter__(self):
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            h = pynvml.nvmlDeviceGetHandleByIndex(self.index)
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(h, pynvml.NVML_CLOCK_SM)
+            names = {
+                "hw_slowdown": getattr(pynvml, "nvmlClocksEventReasonHwSlowdown", 0x8),
+                "hw_thermal_slowdown": getattr(pynvml, "nvmlClocksEventReasonHwThermalSlowdown", 0x40),
+                "sw_thermal_slowdown": getattr(pynvml, "nvmlClocksEventReasonSwThermalSlowdown", 0x20),
+                "sw_power_cap": getattr(pynvml, "nvmlClocksEventReasonSwPowerCap", 0x4),
+                "hw_power_brake_slowdown": getattr(pynvml, "nvmlClocksEventReasonHwPowerBrakeSlowdown", 0x80),
+            }
+
+            def loop():
+                while not self._stop.is_set():
+                    try:
+                        self.samples.append(pynvml.nvmlDeviceGetClockInfo(h, pynvml.NVML_CLOCK_SM))
+                        r = pynvml.nvmlDeviceGetCurrentClocksEventReasons(h)
+                        for n, bit in names.items():
+                            if r & bit:
+                                self.reasons.add(n)
+                    except Exception:
+                        pass
+                    time.sleep(self.period)
+
+            self._thr = threading.Thread(target=loop, daemon=True)
+            self._thr.start()
+        except Exception as e:  # NVML missing: say so in the record
+            self.reasons.add(f"nvml_unavailable:{type(e).__name__}")
+        return self
+
+    def __exit__(self, *a):
+        self._stop.set()
+        if self._thr:
+            self._thr.join()
+
+    def record(self):
+        return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
+                "sm_max_mhz": self.max_mhz, "samples": len(self.samples),
+                "reasons": sorted(self.reasons)}
+
+
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+        return dist, rank, world, local
+    return None, 0, 1, 0
+
+
+def oracle_sample(w, budget_s, max_tasks=None):
+    """Times the fp64 oracle on whole branches (all heads) until ~budget_s of CPU work."""
+    import oracle
+    Hq = w.num_q_heads
+    done_q, t_total, branches = 0, 0.0, 0
+    order = list(range(w.num_branches))
+    for b in order:
+        rows = np.arange(int(w.branch_q_off[b]) * Hq, int(w.branch_q_off[b + 1]) * Hq)
+        t0 = time.perf_counter()
+        oracle.fork_attn(w, rows=rows)
+        t_total += time.perf_counter() - t0
+        done_q += int(w.branch_q_off[b + 1] - w.branch_q_off[b])
+        branches += 1
+        if t_total >= budget_s or (max_tasks and branches >= max_tasks):
+            break
+    return done_q, branches, t_total, oracle.threads_default()
+
+
+def host_copy(w):
+    """Host (pinned) copies of the workload's tensors, for the oracle and the e2e leg."""
+    return (w.q.cpu().pin_memory(), w.k_pages.cpu().pin_memory(), w.v_pages.cpu().pin_memory())
+
+
+def run_reference(args):
+    """The oracle as it stands, on the host cores: one (branch, KV head) task per step."""
+    dist, rank, world, local = dist_setup(args.gpus)
+    if rank != 0:
+        return
+    import oracle
+    dev = "cuda" if torch.cuda.is_available() else "cpu"  # torch's RNG only draws the inputs
+    w = W.make(args.config, device=dev)
+    w.q, w.k_pages, w.v_pages = w.q.cpu(), w.k_pages.cpu(), w.v_pages.cpu()
+    unique_bytes = oracle.unique_slots(w)[0] * w.num_kv_heads * KV_BYTES_PER_SLOT_HEAD
+    Hq, Hkv = w.num_q_heads, w.num_kv_heads
+    G = Hq // Hkv
+    times = []
+    for s in range(args.warmup + args.steps):
+        b = s % w.num_branches
+        g = (s // w.num_branches) % Hkv
+        rows = np.arange(int(w.branch_q_off[b]) * Hq, int(w.branch_q_off[b + 1]) * Hq)
+        rows = rows[(rows % Hq) // G == g]
+        t0 = time.perf_counter()
+        oracle.fork_attn(w, rows=rows)
+        if s >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    sec = sum(times) / len(times)
+    value = unique_bytes / (w.num_branches * Hkv) / sec / 1e9  # prorated share of one call
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "config_id": args.config},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": oracle.threads_default(),
+                             "kind": "oracle",
+                             "sample": "per step one (branch, KV head) of the workload, fp64 "
+                                       "copied-context attention; GB/s prorated by 1/(B*Hkv)"},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args):
+    dist, rank, world, local = dist_setup(args.gpus)
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    w = W.make(args.config, device=str(dev))
+    if rank:
+        w.meta["seed"] += 1000 * rank
+        W.fill_values(w, device=str(dev))  # an independent problem per rank (weak scaling)
+    t0 = time.perf_counter()
+    run = fa.ForkAttention(w, out_dtype=fa.FA_BF16, device=dev)
+    plan_s = time.perf_counter() - t0
+    st = run.plan.stats()
+    unique_bytes = st["unique_visible_slots"] * w.num_kv_heads * KV_BYTES_PER_SLOT_HEAD
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    q, k, v = w.q, w.k_pages, w.v_pages
+
+    def step(events=None):
+        if events is None:
+            fa.fork_attn_decode(q, k, v, run.plan, run.out, run.lse, stream)
+        else:
+            fa.fork_attn_decode_timed(q, k, v, run.plan, run.out, run.lse, events, stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    assert fa.fork_attn_check(run.plan, stream) == 0, "device error word set during warm-up"
+
+    K = args.steps
+    ev_start = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev_stop = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    wall0 = time.perf_counter()
+    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+        for i in range(K):
+            flush.zero_()
+            ev_start[i].record(stream)
+            step(kev[i])
+            ev_stop[i].record(stream)
+        torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - wall0
+    if dist:
+        dist.barrier()
+    step_ms = [a.elapsed_time(b) for a, b in zip(ev_start, ev_stop)]
+    kern_ms = [[kev[i][2 * j].elapsed_time(kev[i][2 * j + 1]) for i in range(K)] for j in range(3)]
+    assert fa.fork_attn_check(run.plan, stream) == 0, "device error word set in the timed region"
+    ms = sum(step_ms) / K
+    ms_max = ms
+    if dist:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_max = float(t.item())
+    value = unique_bytes * world / (ms_max * 1e-3) / 1e9
+    bq_s = w.total_q * world / (ms_max * 1e-3)
+
+    # dominant kernel and its roofline (algorithmic bytes = unique visible slots it reads)
+    names = ["row_kernel", "tcgen05_kernel", "merge_kernel"]
+    avg = [sum(x) / K for x in kern_ms]
+    dom = int(np.argmax(avg))
+    alg = {0: st["unique_slots_rows"], 1: st["unique_slots_tensor"]}.get(dom, 0) * w.num_kv_heads * KV_BYTES_PER_SLOT_HEAD
+    peak, peak_kind = peaks()
+    achieved = alg / (avg[dom] * 1e-3) / 1e9 if avg[dom] > 0 else 0.0
+
+    e2e = None
+    if not args.no_e2e and rank == 0:
+        hq, hk, hv = host_copy(w)
+        out_h = torch.empty(run.out.shape, dtype=run.out.dtype).pin_memory()
+        lse_h = torch.empty(run.lse.shape, dtype=run.lse.dtype).pin_memory()
+        n_e2e = max(3, min(10, K))
+        torch.cuda.synchronize(dev)
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(n_e2e):
+            q.copy_(hq, non_blocking=True)
+            k.copy_(hk, non_blocking=True)
+            v.copy_(hv, non_blocking=True)
+            fa.fork_attn_decode(q, k, v, run.plan, run.out, run.lse, stream)
+            out_h.copy_(run.out, non_blocking=True)
+            lse_h.copy_(run.lse, non_blocking=True)
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = t0.elapsed_time(t1) / n_e2e
+        e2e = {"value": unique_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+               "ms_per_step": e2e_ms,
+               "h2d_bytes_per_step": int(hq.numel() * 2 + hk.numel() * 2 + hv.numel() * 2),
+               "d2h_bytes_per_step": int(out_h.numel() * out_h.element_size() + lse_h.numel() * 4)}
+
+    cpu = None
+    if not args.no_cpu_baseline and rank == 0 and world == 1:
+        hw = W.Workload(**{f: getattr(w, f) for f in ("name", "num_q_heads", "num_kv_heads", "page_ids", "segs",
+                                                       "branch_seg_off", "branch_segs", "branch_q_off",
+                                                       "vis_bits", "vis_word_off", "num_pages_pool")},
+                        meta=dict(w.meta))
+        hw.q, hw.k_pages, hw.v_pages = w.q.cpu(), w.k_pages.cpu(), w.v_pages.cpu()
+        nq, nb, secs, cores = oracle_sample(hw, budget_s=args.cpu_budget)
+        share = nq / w.total_q
+        cpu = {"value": unique_bytes * share / secs / 1e9, "unit": "GB/s", "cores": cores,
+               "kind": "oracle", "branch_queries_per_s": nq / secs,
+               "sample": f"{nb} of {w.num_branches} branches (all heads), fp64 copied-context "
+                         f"attention, {secs:.1f} s; GB/s prorated by the share of query tokens"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "config_id": args.config, "Hq": w.num_q_heads,
+                       "Hkv": w.num_kv_heads, "branches": w.num_branches, "total_q": w.total_q,
+                       "unique_kv_bytes": unique_bytes, "l2": "flushed (256 MiB write) between steps",
+                       "plan_s": plan_s},
+            "branch_queries_per_s": bq_s,
+            "frac_of_hbm_peak": value / world / peak,
+            "roofline": {"bound": "hbm", "kernel": names[dom], "achieved": achieved, "peak": peak,
+                         "unit": "GB/s", "frac": achieved / peak, "traffic": None,
+                         "peak_kind": peak_kind},
+            "kernel_ms": {n: a for n, a in zip(names, avg)},
+            "step_ms_min": min(step_ms), "step_ms_median": statistics.median(step_ms),
+            "wall_s_timed_region": wall,
+            "gpu_launches": K * (int(st["num_items_rows"] > 0) + int(st["num_items_tensor"] > 0)
+                                 + int(st["merge_rows"] > 0)),
+            "clocks": clk.record(),
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+            "gpu": torch.cuda.get_device_name(dev),
+        }
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", type=int, default=4)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,203 @@
+/*
+ * fork_attn.h -- C ABI of libforkattn.so: decode attention over a branching, paged KV cache
+ * on one NVIDIA B300 (sm_103a).
+ *
+ * What the calls compute (sources are the pages' titles and sections):
+ *
+ *   - Octopus (zicq.com, "Octopus以共享KV DAG重构多智能体强化学习"), section "Zero-Copy Radix
+ *     Forking": branches fork from a radix prefix of physical KV pages; a fork adds a cursor,
+ *     not a copy, and the shared pages are read-only.  Here a fork is two branches whose
+ *     segment lists name the same segments (or segments over the same physical pages).
+ *   - Octopus, section "Attention-Only KV Mounting": a thread attends to a sibling's
+ *     terminal KV block in place.  Here a mount is a segment whose pages belong to a sibling,
+ *     listed in the mounting branch's segment list.
+ *   - AKV (news.farwalk.ai, "清华与港中文开源 AKV"), section "AKV 如何工作？": Drop removes
+ *     entries from later attention and keeps positions; Append adds new tokens.  Here a drop
+ *     is a cleared bit in the branch's visibility bits; the query tokens of a branch are its
+ *     last n_q logical tokens (their K/V are already appended).
+ *   - Agentrix (gitlink.org.cn, "Agentrix：面向智能体的内存管理系统设计与实现"), section
+ *     "初赛基础与决赛演进", CUDA ForkAttention: the cached pages are split into a common part
+ *     and private parts, many queries reuse one read of the common KV, and per-branch results
+ *     are merged.  Here: the planner groups page runs by reader set, the kernels read every
+ *     visible physical page once per KV head and row group, and a log-sum-exp merge joins
+ *     the partial results.
+ *
+ * Result, for branch b with logical sequence of length n_b and query token i (position
+ * p = n_b - n_q_b + i), query head h, KV head g = h / (Hq / Hkv), and visible set
+ * V = { j <= p : vis_b[j] = 1 }:
+ *     s_j = scale * <q[b,i,h], K[slot(j), g]>
+ *     lse[b,i,h] = ln sum_{j in V} exp(s_j)                     (natural log, scale included)
+ *     out[b,i,h] = sum_{j in V} exp(s_j - lse) * V[slot(j), g]
+ * An empty V gives out = 0 and lse = -inf.
+ *
+ * Conventions common to every call:
+ *   - Every function returns an int status: FA_OK (0) or a negative FA_ERR_*; none aborts.
+ *     fork_attn_strerror() names a status.
+ *   - Host pointers are marked [host], device pointers [device].  The library never
+ *     allocates device memory: the caller owns every device buffer (inputs, outputs, plan
+ *     buffer and scratch) and keeps it alive while work that uses it may run.
+ *   - A stream argument is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *   - Only head_dim = 128 and page_size = 16 are built; other values return
+ *     FA_ERR_UNSUPPORTED.
+ */
+#ifndef FORK_ATTN_H
+#define FORK_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+    FA_OK = 0,
+    FA_ERR_NULL = -1,          /* a required pointer is NULL                                  */
+    FA_ERR_INVALID = -2,       /* malformed descriptor or dims (see fork_attn_plan_create)   */
+    FA_ERR_UNSUPPORTED = -3,   /* head_dim / page_size / GQA shape not built                  */
+    FA_ERR_RANGE = -4,         /* an index (page id, segment id, offset) is out of range     */
+    FA_ERR_ALIGN = -5,         /* a device pointer is not 16-byte aligned                    */
+    FA_ERR_NOT_UPLOADED = -6,  /* fork_attn_decode before fork_attn_plan_upload               */
+    FA_ERR_CUDA = -7,          /* a CUDA runtime / driver call failed                         */
+    FA_ERR_NOMEM = -8,         /* host allocation failed                                      */
+    FA_ERR_BUFFER_SMALL = -9,  /* a caller buffer is smaller than fork_attn_plan_sizes says   */
+    FA_ERR_DEVICE = -10        /* a kernel reported a fault through the plan's error word     */
+};
+
+enum { FA_BF16 = 0, FA_F32 = 1 };
+
+/* Problem dimensions.  num_q_heads % num_kv_heads == 0 (GQA group G = num_q_heads /
+ * num_kv_heads, query head h reads KV head h / G).  scale multiplies q.k (1/sqrt(128) in the
+ * workloads).  out_dtype selects the element type of `out` in fork_attn_decode. */
+typedef struct {
+    int32_t num_q_heads;
+    int32_t num_kv_heads;
+    int32_t head_dim;   /* must be 128 */
+    int32_t page_size;  /* must be 16  */
+    float scale;
+    int32_t out_dtype;  /* FA_BF16 or FA_F32 */
+} fa_dims;
+
+/* A segment: `len` consecutive tokens, starting at slot `tok_begin` of the listed page
+ * page_ids[page_off]; token t sits in page page_ids[page_off + (tok_begin + t) / page_size],
+ * slot (tok_begin + t) % page_size. */
+typedef struct {
+    int32_t page_off;   /* index into page_ids of the segment's first page   */
+    int32_t tok_begin;  /* 0 .. page_size-1                                  */
+    int32_t len;        /* >= 1                                              */
+} fa_segment;
+
+/* The branching cache, all in [host] memory owned by the caller and read only during
+ * fork_attn_plan_create.  Branch b's logical sequence is the concatenation of segments
+ * branch_segs[branch_seg_off[b] .. branch_seg_off[b+1]) in list order; a segment may be
+ * listed by many branches (a fork or a mount) and even twice by one (it then counts twice). */
+typedef struct {
+    const int32_t *page_ids;        /* [num_page_ids] physical page per listed page          */
+    int64_t num_page_ids;
+    const fa_segment *segs;         /* [num_segs]                                            */
+    int32_t num_segs;
+    const int32_t *branch_seg_off;  /* [num_branches + 1], branch_seg_off[0] = 0, ascending  */
+    const int32_t *branch_segs;     /* segment ids                                           */
+    int32_t num_branches;           /* >= 1                                                  */
+    const int32_t *branch_q_off;    /* [num_branches + 1] query tokens per branch (CSR);     */
+                                    /* NULL = one query token per branch.  1 <= n_q <= n_b.   */
+    const uint32_t *vis_bits;       /* visibility bits, bit j%32 of word vis_word_off[b] +   */
+    const int64_t *vis_word_off;    /* j/32 for logical index j of branch b; 1 = visible.    */
+                                    /* Both NULL = everything visible.                        */
+    int64_t num_vis_words;          /* length of vis_bits (bounds vis_word_off[b] + n_b/32)  */
+    int64_t num_pages_pool;         /* physical page ids must lie in [0, num_pages_pool)     */
+} fa_desc;
+
+/* Planner knobs; pass NULL to fork_attn_plan_create for the defaults (all fields 0). */
+typedef struct {
+    int32_t chunk_pages;    /* max pages per work chunk (0 = chosen from the SM count)      */
+    int32_t num_sms;        /* SMs to plan for (0 = 148)                                     */
+    int32_t tensor_min_rows;/* reader-set rows at which a run goes to the tcgen05 kernel    */
+                            /* (0 = default; < 0 = never)                                    */
+    int32_t reserved[5];
+} fa_plan_opts;
+
+/* Counters of a plan, for measurement.  unique_visible_slots: distinct physical token slots
+ * visible to at least one query (a slot read by many branches counts once); touched_pages:
+ * distinct physical pages holding such a slot.  One slot of one KV head is 2 x 128 x 2 bytes
+ * of K and V. */
+typedef struct {
+    int64_t unique_visible_slots;
+    int64_t touched_pages;
+    int64_t listed_visible_slots;  /* sum over branches of visible entries (copy-context)   */
+    int64_t num_chunks;
+    int64_t num_items_rows;        /* work items of the CUDA-core/mma.sync row kernel       */
+    int64_t num_items_tensor;      /* work items of the tcgen05 kernel                      */
+    int64_t kv_bytes_rows;         /* K+V bytes read by the row kernel (all heads)           */
+    int64_t kv_bytes_tensor;       /* K+V bytes read by the tcgen05 kernel                   */
+    int64_t partial_rows;          /* fp32 partial (out, lse) rows in scratch                */
+    int64_t merge_rows;            /* (query token, head) rows merged by the merge kernel   */
+    int64_t total_q;
+    int64_t unique_slots_rows;     /* distinct visible physical slots read by the row kernel */
+    int64_t unique_slots_tensor;   /* distinct visible physical slots read by tcgen05 kernel */
+    int64_t reserved[3];
+} fa_plan_stats;
+
+typedef struct fa_plan fa_plan; /* opaque; owned by the library */
+
+/* Builds a plan on the host: validates dims and descriptor, finds runs of physical pages
+ * with the same reader set, skips pages no reader sees, cuts runs into chunks, assigns
+ * partial-result rows and packs per-chunk visibility words.  Errors: FA_ERR_NULL,
+ * FA_ERR_INVALID (bad CSR, n_q outside [1, n_b], empty branch, bad scale/out_dtype),
+ * FA_ERR_RANGE (segment id, page offset or page id out of range, bit array too short),
+ * FA_ERR_UNSUPPORTED (head_dim != 128, page_size != 16, Hq % Hkv != 0, G > 32),
+ * FA_ERR_NOMEM.  *out_plan is set only on FA_OK. */
+int fork_attn_plan_create(const fa_dims *dims, const fa_desc *desc, const fa_plan_opts *opts,
+                          fa_plan **out_plan);
+
+/* Byte sizes of the two device buffers the caller must provide to fork_attn_plan_upload:
+ * plan_bytes for the plan arrays, scratch_bytes for fp32 partial results (may be 0). */
+int fork_attn_plan_sizes(const fa_plan *plan, size_t *plan_bytes, size_t *scratch_bytes);
+
+/* Fills *stats [host]. */
+int fork_attn_plan_stats(const fa_plan *plan, fa_plan_stats *stats);
+
+/* Copies the plan arrays into dev_plan_buf [device, 256-byte aligned, >= plan_bytes] on
+ * `stream` and records both buffers in the plan for later decodes.  dev_scratch_buf
+ * [device, 256-byte aligned, >= scratch_bytes] may be NULL when scratch_bytes is 0.  The
+ * host copy is synchronous with respect to the host.  Errors: FA_ERR_NULL, FA_ERR_ALIGN,
+ * FA_ERR_BUFFER_SMALL, FA_ERR_CUDA. */
+int fork_attn_plan_upload(fa_plan *plan, void *dev_plan_buf, size_t plan_buf_bytes,
+                          void *dev_scratch_buf, size_t scratch_buf_bytes, void *stream);
+
+/* Runs the decode on `stream`: no allocation, no host synchronisation.
+ *   q       [device] bf16 [total_q][num_q_heads][128]; total_q = branch_q_off[B]; query token
+ *           i of branch b is row branch_q_off[b] + i.
+ *   k_pages [device] bf16 [num_pages_pool][num_kv_heads][16][128]
+ *   v_pages [device] same layout as k_pages
+ *   out     [device] out_dtype [total_q][num_q_heads][128]
+ *   lse     [device] fp32 [total_q][num_q_heads]  (natural log)
+ * All device pointers must be 16-byte aligned.  Inputs are only read.  Errors: FA_ERR_NULL,
+ * FA_ERR_ALIGN, FA_ERR_NOT_UPLOADED, FA_ERR_CUDA (launch failure). */
+int fork_attn_decode(const void *q, const void *k_pages, const void *v_pages,
+                     const fa_plan *plan, void *out, float *lse, void *stream);
+
+/* Like fork_attn_decode; if `events` [host] is not NULL it is an array of 2*n_events
+ * cudaEvent_t handles (as void*) recorded on `stream` around each kernel launch, in launch
+ * order: [start_0, stop_0, start_1, stop_1, ...] for the row kernel, the tcgen05 kernel and
+ * the merge kernel (an absent kernel records start = stop).  n_events must be 0 or 3. */
+int fork_attn_decode_timed(const void *q, const void *k_pages, const void *v_pages,
+                           const fa_plan *plan, void *out, float *lse, void *stream,
+                           void **events, int32_t n_events);
+
+/* Reads the plan's device error word on `stream` (synchronising it) into *device_error [host]
+ * and clears it.  A non-zero word means a kernel gave up (an expired wait or a failed check)
+ * and the outputs of that decode are not valid. */
+int fork_attn_check(fa_plan *plan, int32_t *device_error, void *stream);
+
+/* Frees the host plan.  Device buffers stay owned by the caller. */
+int fork_attn_plan_destroy(fa_plan *plan);
+
+/* A static string for a status code. */
+const char *fork_attn_strerror(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FORK_ATTN_H */

@@ -1,0 +1,183 @@
+// Launcher side of the C ABI: plan upload, tensor-map encoding, kernel launches, error word.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstring>
+#include <mutex>
+
+#include "merge_kernel.cuh"
+#include "plan_internal.h"
+#include "row_kernel.cuh"
+
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+// Pages [pool][Hkv][16][128] bf16 seen as a 4-D tensor (dims innermost first), read in boxes
+// of 64 dims x 16 tokens of one head of one page, 128-byte swizzled in shared memory.
+bool encode_pages(CUtensorMap *map, const void *pages, int64_t pool, int32_t hkv) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[4] = {cuuint64_t(fa::kHeadDim), cuuint64_t(fa::kPageSize), cuuint64_t(hkv),
+                                cuuint64_t(pool)};
+    const cuuint64_t strides[3] = {cuuint64_t(fa::kHeadDim * 2), cuuint64_t(fa::kPageSize * fa::kHeadDim * 2),
+                                   cuuint64_t(hkv) * fa::kPageSize * fa::kHeadDim * 2};
+    const cuuint32_t box[4] = {64, cuuint32_t(fa::kPageSize), 1, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(pages), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+int set_smem_attr() {
+    // once per device: the row kernel needs more than the default 48 KiB of dynamic smem
+    static std::mutex mu;
+    static bool done[128] = {false};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return FA_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(mu);
+    if (!done[dev]) {
+        if (cudaFuncSetAttribute(fa::rowk::row_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(fa::rowk::kSmemBytes)) != cudaSuccess)
+            return FA_ERR_CUDA;
+        done[dev] = true;
+    }
+    return FA_OK;
+}
+
+int fill_params(const fa_plan *plan, const void *q, const void *k_pages, const void *v_pages, void *out,
+                float *lse, void *scratch, fa::DecodeParams &p) {
+    std::memset(&p, 0, sizeof p);
+    if (!encode_pages(&p.kmap, k_pages, plan->num_pages_pool, plan->dims.num_kv_heads) ||
+        !encode_pages(&p.vmap, v_pages, plan->num_pages_pool, plan->dims.num_kv_heads))
+        return FA_ERR_CUDA;
+    const fa::Layout &L = plan->lay;
+    uint8_t *base = static_cast<uint8_t *>(plan->dev_plan);
+    p.q = static_cast<const __nv_bfloat16 *>(q);
+    p.out = out;
+    p.lse = lse;
+    p.part_o = static_cast<float *>(scratch);
+    p.part_lse = scratch ? reinterpret_cast<float *>(static_cast<uint8_t *>(scratch) +
+                                                     fa::scratch_lse_offset(plan->partial_rows))
+                         : nullptr;
+    p.chunk_pages = reinterpret_cast<const int32_t *>(base + L.chunk_pages);
+    p.chunks = reinterpret_cast<const fa::Chunk *>(base + L.chunks);
+    p.occs = reinterpret_cast<const fa::Occ *>(base + L.occs);
+    p.items = reinterpret_cast<const fa::Item *>(base + L.items_rows);
+    p.ents = reinterpret_cast<const fa::Ent *>(base + L.ents);
+    p.branches = reinterpret_cast<const fa::Branch *>(base + L.branches);
+    p.q_branch = reinterpret_cast<const int32_t *>(base + L.q_branch);
+    p.merge_bases = reinterpret_cast<const int32_t *>(base + L.merge_bases);
+    p.mask_words = reinterpret_cast<const uint32_t *>(base + L.mask_words);
+    p.err = reinterpret_cast<int32_t *>(base);
+    p.Hq = plan->dims.num_q_heads;
+    p.Hkv = plan->dims.num_kv_heads;
+    p.G = plan->G;
+    p.out_dtype = plan->dims.out_dtype;
+    p.scale_log2 = plan->dims.scale * 1.4426950408889634f;
+    p.n_items = L.n_items_rows;
+    p.total_rows = L.total_q * plan->dims.num_q_heads;
+    return FA_OK;
+}
+
+bool needs_merge(const fa_plan *plan) { return plan->stats.merge_rows > 0; }
+
+int launch_all(const fa::DecodeParams &p, const fa_plan *plan, cudaStream_t st, void **events) {
+    auto rec = [&](int i) {
+        if (events) cudaEventRecord(static_cast<cudaEvent_t>(events[i]), st);
+    };
+    rec(0);
+    if (p.n_items > 0)
+        fa::rowk::row_kernel<<<p.n_items, fa::rowk::kThreads, fa::rowk::kSmemBytes, st>>>(p);
+    rec(1);
+    rec(2);  // tcgen05 kernel slot (no items in this plan)
+    rec(3);
+    rec(4);
+    if (needs_merge(plan)) {
+        const int64_t threads = int64_t(p.total_rows) * 32;
+        const int blocks = int((threads + fa::mergek::kThreads - 1) / fa::mergek::kThreads);
+        fa::mergek::merge_kernel<<<blocks, fa::mergek::kThreads, 0, st>>>(p);
+    }
+    rec(5);
+    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" int fork_attn_plan_upload(fa_plan *plan, void *dev_plan_buf, size_t plan_buf_bytes,
+                                     void *dev_scratch_buf, size_t scratch_buf_bytes, void *stream) {
+    if (!plan || !dev_plan_buf) return FA_ERR_NULL;
+    const size_t need_plan = size_t(plan->lay.total);
+    const size_t need_scratch = size_t(fa::scratch_bytes(plan->partial_rows));
+    if (!aligned(dev_plan_buf, fa::kAlign)) return FA_ERR_ALIGN;
+    if (plan_buf_bytes < need_plan) return FA_ERR_BUFFER_SMALL;
+    if (need_scratch > 0) {
+        if (!dev_scratch_buf) return FA_ERR_NULL;
+        if (!aligned(dev_scratch_buf, fa::kAlign)) return FA_ERR_ALIGN;
+        if (scratch_buf_bytes < need_scratch) return FA_ERR_BUFFER_SMALL;
+    }
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(dev_plan_buf, plan->blob.data(), need_plan, cudaMemcpyHostToDevice, st) != cudaSuccess)
+        return FA_ERR_CUDA;
+    plan->dev_plan = dev_plan_buf;
+    plan->dev_scratch = dev_scratch_buf;
+    plan->uploaded = true;
+    return FA_OK;
+}
+
+extern "C" int fork_attn_decode_timed(const void *q, const void *k_pages, const void *v_pages,
+                                      const fa_plan *plan, void *out, float *lse, void *stream,
+                                      void **events, int32_t n_events) {
+    if (!plan || !q || !k_pages || !v_pages || !out || !lse) return FA_ERR_NULL;
+    if (!plan->uploaded) return FA_ERR_NOT_UPLOADED;
+    if (!aligned(q, 16) || !aligned(k_pages, 16) || !aligned(v_pages, 16) || !aligned(out, 16) ||
+        !aligned(lse, 16))
+        return FA_ERR_ALIGN;
+    if (events && n_events != 3) return FA_ERR_INVALID;
+    int rc = set_smem_attr();
+    if (rc != FA_OK) return rc;
+    fa::DecodeParams p;
+    rc = fill_params(plan, q, k_pages, v_pages, out, lse, plan->dev_scratch, p);
+    if (rc != FA_OK) return rc;
+    return launch_all(p, plan, static_cast<cudaStream_t>(stream), events);
+}
+
+extern "C" int fork_attn_decode(const void *q, const void *k_pages, const void *v_pages,
+                                const fa_plan *plan, void *out, float *lse, void *stream) {
+    return fork_attn_decode_timed(q, k_pages, v_pages, plan, out, lse, stream, nullptr, 0);
+}
+
+extern "C" int fork_attn_check(fa_plan *plan, int32_t *device_error, void *stream) {
+    if (!plan || !device_error) return FA_ERR_NULL;
+    if (!plan->uploaded) return FA_ERR_NOT_UPLOADED;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int32_t word = 0;
+    if (cudaMemcpyAsync(&word, plan->dev_plan, sizeof word, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+        return FA_ERR_CUDA;
+    *device_error = word;
+    if (word != 0) {
+        if (cudaMemsetAsync(plan->dev_plan, 0, sizeof word, st) != cudaSuccess) return FA_ERR_CUDA;
+        return FA_ERR_DEVICE;
+    }
+    return FA_OK;
+}

@@ -1,0 +1,35 @@
+// Kernel parameter block shared by the decode kernels (passed by value as a grid constant).
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include "../../include/fork_attn.h"
+#include "plan_layout.h"
+
+namespace fa {
+
+struct DecodeParams {
+    CUtensorMap kmap;  // K pages viewed as [pages][Hkv][16][128] bf16, box 64 x 16, 128B swizzle
+    CUtensorMap vmap;  // same for V
+    const __nv_bfloat16 *q;
+    void *out;
+    float *lse;
+    float *part_o;    // [partial_rows][128] fp32
+    float *part_lse;  // [partial_rows] fp32, natural log
+    const int32_t *chunk_pages;
+    const Chunk *chunks;
+    const Occ *occs;
+    const Item *items;
+    const Ent *ents;
+    const Branch *branches;
+    const int32_t *q_branch;
+    const int32_t *merge_bases;
+    const uint32_t *mask_words;
+    int32_t *err;
+    int32_t Hq, Hkv, G, out_dtype;
+    float scale_log2;  // scale * log2(e): scores are kept in base 2 inside the kernels
+    int32_t n_items;
+    int32_t total_rows;  // total_q * Hq
+};
+
+}  // namespace fa

@@ -1,0 +1,53 @@
+// Log-sum-exp merge of partial results.
+//
+// Agentrix (gitlink.org.cn), section "初赛基础与决赛演进", CUDA ForkAttention: after the
+// common part is computed once for all branches and the private parts per branch, each
+// branch's results are merged.  For a (query token, query head) row with partials
+// (O_k, lse_k) over disjoint sets of entries:
+//     L = max_k lse_k + ln sum_k exp(lse_k - max_k lse_k),    O = sum_k exp(lse_k - L) O_k.
+// One warp per row; each lane owns 4 of the 128 dims; partials are visited in the plan's
+// fixed order, so the result is bitwise run-to-run deterministic.
+#pragma once
+#include "decode_params.cuh"
+#include "ptx.cuh"
+
+namespace fa {
+namespace mergek {
+
+constexpr int kThreads = 256;
+
+__global__ void __launch_bounds__(kThreads) merge_kernel(const __grid_constant__ DecodeParams p) {
+    const int row = int((blockIdx.x * size_t(kThreads) + threadIdx.x) >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= p.total_rows) return;
+    const int qt = row / p.Hq, h = row % p.Hq;
+    const Branch br = p.branches[p.q_branch[qt]];
+    if (br.direct) return;  // its only chunk wrote the output
+    const int i = qt - br.q_begin, g = h / p.G, jh = h % p.G;
+    const int off = g * (br.n_q * p.G) + i * p.G + jh;
+    float M = -INFINITY;
+    for (int k = 0; k < br.n_merge; ++k) M = fmaxf(M, p.part_lse[p.merge_bases[br.merge_off + k] + off]);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float L = 0.f;
+    if (M != -INFINITY) {
+        for (int k = 0; k < br.n_merge; ++k) {
+            const int prow = p.merge_bases[br.merge_off + k] + off;
+            const float w = expf(p.part_lse[prow] - M);
+            const float4 v = *reinterpret_cast<const float4 *>(p.part_o + size_t(prow) * kHeadDim + lane * 4);
+            L += w;
+            acc.x += w * v.x; acc.y += w * v.y; acc.z += w * v.z; acc.w += w * v.w;
+        }
+        const float inv = 1.f / L;
+        acc.x *= inv; acc.y *= inv; acc.z *= inv; acc.w *= inv;
+    }
+    if (p.out_dtype == FA_F32) {
+        *reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.out) + size_t(row) * kHeadDim + lane * 4) = acc;
+    } else {
+        uint2 pk = make_uint2(ptx::pack_bf16(acc.x, acc.y), ptx::pack_bf16(acc.z, acc.w));
+        *reinterpret_cast<uint2 *>(reinterpret_cast<__nv_bfloat16 *>(p.out) + size_t(row) * kHeadDim + lane * 4) = pk;
+    }
+    if (lane == 0) p.lse[row] = (M == -INFINITY) ? -INFINITY : M + logf(L);
+}
+
+}  // namespace mergek
+}  // namespace fa

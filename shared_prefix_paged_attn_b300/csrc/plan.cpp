@@ -1,0 +1,490 @@
+// Host planner for fork decode attention over a branching, paged KV cache.
+//
+// Agentrix (gitlink.org.cn), section "初赛基础与决赛演进", CUDA ForkAttention: the cache is
+// split by the pages actually shared into a common part and private parts, the common KV is
+// read once for many queries, and per-branch results are merged.  Octopus (zicq.com),
+// section "Packed DAG-GRPO", notes that real speed depends on page layout, block-table
+// organisation, occupancy and branch imbalance; the planner is where those are decided.
+//
+// Steps:
+//   1. validate the dims and the descriptor (every index is range-checked here, once);
+//   2. walk every branch's segments and emit one record per (physical page, reader), where a
+//      reader is a branch at a given logical offset; the record carries the 16 visibility
+//      bits of that page for that reader (slot in the segment and not dropped);
+//   3. group records by physical page: a page's reader set is all of its records;
+//   4. chain pages into runs: page p' follows p when every reader of p reads p' at the next
+//      16 logical positions and nobody else reads p' (equal reader sets); pages that no
+//      reader sees at all are skipped, and end a run;
+//   5. cut runs into chunks (long enough that fp32 partial results stay a few percent of the
+//      KV bytes, short enough for occupancy), pack per-reader visibility words, give every
+//      (chunk, reader) its partial rows (or a direct write when it is the branch's only one);
+//   6. emit work items = chunk x KV head x row group and the per-branch merge lists.
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "plan_internal.h"
+
+namespace {
+
+using fa::kPageSize;
+
+struct Rec {
+    int32_t page;
+    int32_t branch;
+    int32_t lpos0;  // logical position of the page's slot 0 for this reader
+    uint32_t vis;   // 16 bits: slot in the segment and visible
+};
+
+struct Input {
+    const fa_dims *d;
+    const fa_desc *s;
+    int32_t G;
+    std::vector<int64_t> n_b;
+    std::vector<int32_t> q_off;
+};
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+int64_t align_up(int64_t a) { return ceil_div(a, fa::kAlign) * fa::kAlign; }
+
+int validate(Input &in) {
+    const fa_dims *d = in.d;
+    const fa_desc *s = in.s;
+    if (d->head_dim != fa::kHeadDim || d->page_size != kPageSize) return FA_ERR_UNSUPPORTED;
+    if (d->num_q_heads < 1 || d->num_kv_heads < 1) return FA_ERR_INVALID;
+    if (d->num_q_heads % d->num_kv_heads) return FA_ERR_UNSUPPORTED;
+    in.G = d->num_q_heads / d->num_kv_heads;
+    if (in.G > fa::kRowsMax) return FA_ERR_UNSUPPORTED;
+    if (!(d->scale > 0.0f) || !std::isfinite(d->scale)) return FA_ERR_INVALID;
+    if (d->out_dtype != FA_BF16 && d->out_dtype != FA_F32) return FA_ERR_INVALID;
+    if (s->num_branches < 1 || s->num_pages_pool < 1 || s->num_segs < 0 || s->num_page_ids < 0)
+        return FA_ERR_INVALID;
+    if (s->num_pages_pool > (int64_t(1) << 31) - 1) return FA_ERR_RANGE;
+    if (!s->branch_seg_off || !s->branch_segs) return FA_ERR_NULL;
+    if ((s->num_segs > 0 && !s->segs) || (s->num_page_ids > 0 && !s->page_ids)) return FA_ERR_NULL;
+    if ((s->vis_bits == nullptr) != (s->vis_word_off == nullptr)) return FA_ERR_INVALID;
+    for (int64_t i = 0; i < s->num_page_ids; ++i)
+        if (s->page_ids[i] < 0 || s->page_ids[i] >= s->num_pages_pool) return FA_ERR_RANGE;
+    for (int32_t i = 0; i < s->num_segs; ++i) {
+        const fa_segment &g = s->segs[i];
+        if (g.len < 1) return FA_ERR_INVALID;
+        if (g.tok_begin < 0 || g.tok_begin >= kPageSize || g.page_off < 0) return FA_ERR_RANGE;
+        if (g.page_off + ceil_div(int64_t(g.tok_begin) + g.len, kPageSize) > s->num_page_ids)
+            return FA_ERR_RANGE;
+    }
+    const int32_t B = s->num_branches;
+    if (s->branch_seg_off[0] != 0) return FA_ERR_INVALID;
+    in.n_b.assign(B, 0);
+    for (int32_t b = 0; b < B; ++b) {
+        const int32_t e0 = s->branch_seg_off[b], e1 = s->branch_seg_off[b + 1];
+        if (e1 <= e0) return FA_ERR_INVALID;  // an empty branch has no query token
+        for (int32_t e = e0; e < e1; ++e) {
+            const int32_t sg = s->branch_segs[e];
+            if (sg < 0 || sg >= s->num_segs) return FA_ERR_RANGE;
+            in.n_b[b] += s->segs[sg].len;
+        }
+        if (in.n_b[b] > (int64_t(1) << 30)) return FA_ERR_INVALID;
+    }
+    in.q_off.assign(B + 1, 0);
+    for (int32_t b = 0; b < B; ++b) {
+        const int64_t nq = s->branch_q_off ? int64_t(s->branch_q_off[b + 1]) - s->branch_q_off[b] : 1;
+        if (s->branch_q_off && s->branch_q_off[0] != 0) return FA_ERR_INVALID;
+        if (nq < 1 || nq > in.n_b[b]) return FA_ERR_INVALID;
+        in.q_off[b + 1] = int32_t(in.q_off[b] + nq);
+        if (int64_t(in.q_off[b]) + nq > (int64_t(1) << 30)) return FA_ERR_INVALID;
+    }
+    if (s->vis_bits) {
+        if (s->num_vis_words < 0) return FA_ERR_INVALID;
+        for (int32_t b = 0; b < B; ++b) {
+            const int64_t w0 = s->vis_word_off[b];
+            if (w0 < 0 || w0 + ceil_div(in.n_b[b], 32) > s->num_vis_words) return FA_ERR_RANGE;
+        }
+    }
+    return FA_OK;
+}
+
+struct Builder {
+    Input &in;
+    std::vector<Rec> recs;            // in (branch, logical) order
+    std::vector<int64_t> branch_rec;  // CSR into recs per branch
+    std::vector<int32_t> by_page;     // record ids sorted by (page, branch, lpos0)
+    std::vector<int32_t> group_start, group_count, group_of_page;
+    std::vector<uint32_t> group_union;
+
+    explicit Builder(Input &i) : in(i) {}
+
+    bool visible(int32_t b, int64_t j) const {
+        const fa_desc *s = in.s;
+        if (!s->vis_bits) return true;
+        const uint32_t w = s->vis_bits[s->vis_word_off[b] + (j >> 5)];
+        return (w >> (j & 31)) & 1u;
+    }
+
+    void emit_records() {
+        const fa_desc *s = in.s;
+        branch_rec.assign(s->num_branches + 1, 0);
+        for (int32_t b = 0; b < s->num_branches; ++b) {
+            int64_t L = 0;
+            for (int32_t e = s->branch_seg_off[b]; e < s->branch_seg_off[b + 1]; ++e) {
+                const fa_segment &g = s->segs[s->branch_segs[e]];
+                const int64_t n_pages = ceil_div(int64_t(g.tok_begin) + g.len, kPageSize);
+                for (int64_t k = 0; k < n_pages; ++k) {
+                    const int32_t page = s->page_ids[g.page_off + k];
+                    const int64_t lo = (k == 0) ? g.tok_begin : 0;
+                    const int64_t hi = std::min<int64_t>(kPageSize, g.tok_begin + int64_t(g.len) - kPageSize * k);
+                    const int64_t lpos0 = L + kPageSize * k - g.tok_begin;
+                    uint32_t vis = 0;
+                    for (int64_t sl = lo; sl < hi; ++sl)
+                        if (visible(b, lpos0 + sl)) vis |= 1u << sl;
+                    if (!recs.empty() && int64_t(recs.size()) > branch_rec[b] &&
+                        recs.back().page == page && recs.back().lpos0 == lpos0) {
+                        recs.back().vis |= vis;  // a segment boundary inside one page
+                    } else {
+                        recs.push_back(Rec{page, b, int32_t(lpos0), vis});
+                    }
+                }
+                L += g.len;
+            }
+            branch_rec[b + 1] = int64_t(recs.size());
+        }
+    }
+
+    void group_by_page() {
+        const int32_t n = int32_t(recs.size());
+        by_page.resize(n);
+        for (int32_t i = 0; i < n; ++i) by_page[i] = i;
+        std::sort(by_page.begin(), by_page.end(), [&](int32_t a, int32_t b) {
+            const Rec &x = recs[a], &y = recs[b];
+            if (x.page != y.page) return x.page < y.page;
+            if (x.branch != y.branch) return x.branch < y.branch;
+            return x.lpos0 < y.lpos0;
+        });
+        group_of_page.assign(in.s->num_pages_pool, -1);
+        for (int32_t i = 0; i < n;) {
+            int32_t j = i;
+            uint32_t u = 0;
+            while (j < n && recs[by_page[j]].page == recs[by_page[i]].page) u |= recs[by_page[j++]].vis;
+            group_of_page[recs[by_page[i]].page] = int32_t(group_start.size());
+            group_start.push_back(i);
+            group_count.push_back(j - i);
+            group_union.push_back(u);
+            i = j;
+        }
+    }
+
+    // p1 continues p0 when the reader lists match with every logical offset advanced by 16.
+    bool chains(int32_t g0, int32_t g1) const {
+        if (group_count[g0] != group_count[g1]) return false;
+        for (int32_t t = 0; t < group_count[g0]; ++t) {
+            const Rec &a = recs[by_page[group_start[g0] + t]];
+            const Rec &b = recs[by_page[group_start[g1] + t]];
+            if (a.branch != b.branch || int64_t(b.lpos0) != int64_t(a.lpos0) + kPageSize) return false;
+        }
+        return true;
+    }
+
+    std::vector<std::vector<int32_t>> build_runs() {
+        std::vector<std::vector<int32_t>> runs;
+        std::vector<char> assigned(group_start.size(), 0);
+        for (int32_t b = 0; b < in.s->num_branches; ++b) {
+            for (int64_t r = branch_rec[b]; r < branch_rec[b + 1]; ++r) {
+                const int32_t g = group_of_page[recs[r].page];
+                if (assigned[g]) continue;
+                assigned[g] = 1;
+                if (group_union[g] == 0) continue;  // no reader sees this page: never read it
+                std::vector<int32_t> run{g};
+                int64_t cur = r;
+                while (cur + 1 < branch_rec[b + 1]) {
+                    const Rec &nx = recs[cur + 1];
+                    if (int64_t(nx.lpos0) != int64_t(recs[cur].lpos0) + kPageSize) break;
+                    const int32_t g1 = group_of_page[nx.page];
+                    if (assigned[g1] || group_union[g1] == 0 || !chains(run.back(), g1)) break;
+                    assigned[g1] = 1;
+                    run.push_back(g1);
+                    ++cur;
+                }
+                runs.push_back(std::move(run));
+            }
+        }
+        return runs;
+    }
+};
+
+struct Emit {
+    std::vector<int32_t> chunk_pages;
+    std::vector<fa::Chunk> chunks;
+    std::vector<fa::Occ> occs;
+    std::vector<fa::Item> items_rows, items_tc;
+    std::vector<fa::Ent> ents;
+    std::vector<fa::Branch> branches;
+    std::vector<int32_t> q_branch, merge_bases;
+    std::vector<uint32_t> mask_words;
+};
+
+int build_plan(Input &in, const fa_plan_opts &opts, fa_plan *plan) {
+    Builder bd(in);
+    bd.emit_records();
+    bd.group_by_page();
+    std::vector<std::vector<int32_t>> runs = bd.build_runs();
+
+    const fa_desc *s = in.s;
+    const int32_t B = s->num_branches, G = in.G, Hkv = in.d->num_kv_heads;
+    const int32_t base_pages = opts.chunk_pages > 0 ? opts.chunk_pages : 32;
+    Emit em;
+    fa_plan_stats &st = plan->stats;
+    std::memset(&st, 0, sizeof st);
+
+    std::vector<int32_t> occ_count(B, 0);
+    for (const auto &run : runs) {
+        const int32_t g0 = run[0];
+        const int32_t n_read = bd.group_count[g0];
+        int64_t rows = 0;
+        for (int32_t t = 0; t < n_read; ++t) {
+            const Rec &rd = bd.recs[bd.by_page[bd.group_start[g0] + t]];
+            rows += int64_t(in.q_off[rd.branch + 1] - in.q_off[rd.branch]) * G;
+        }
+        // fp32 partial rows cost rows * 1 KiB (write + read) per chunk and KV head; a chunk of
+        // n pages carries n * 8 KiB of K+V, so n >= 2 * rows keeps partials near 6% of KV.
+        int64_t target = std::max<int64_t>(base_pages, 2 * rows);
+        if (opts.chunk_pages > 0) target = opts.chunk_pages;
+        target = std::min<int64_t>(target, 256);
+        const int64_t n = int64_t(run.size());
+        const int64_t n_ch = std::max<int64_t>(1, ceil_div(n, target));
+        int64_t pos = 0;
+        for (int64_t c = 0; c < n_ch; ++c) {
+            const int64_t len = n / n_ch + (c < n % n_ch ? 1 : 0);
+            fa::Chunk ch;
+            ch.page_off = int32_t(em.chunk_pages.size());
+            ch.n_pages = int32_t(len);
+            ch.occ_off = int32_t(em.occs.size());
+            ch.n_occ = n_read;
+            for (int64_t k = 0; k < len; ++k) {
+                const int32_t g = run[pos + k];
+                em.chunk_pages.push_back(bd.recs[bd.by_page[bd.group_start[g]]].page);
+                st.unique_visible_slots += __builtin_popcount(bd.group_union[g]);
+                st.unique_slots_rows += __builtin_popcount(bd.group_union[g]);
+                st.touched_pages += 1;
+                for (int32_t t = 0; t < n_read; ++t)
+                    st.listed_visible_slots += __builtin_popcount(bd.recs[bd.by_page[bd.group_start[g] + t]].vis);
+            }
+            for (int32_t t = 0; t < n_read; ++t) {
+                const Rec &rd = bd.recs[bd.by_page[bd.group_start[run[pos]] + t]];
+                fa::Occ oc;
+                oc.branch = rd.branch;
+                oc.lpos0 = rd.lpos0;
+                oc.prow_base = 0;  // assigned below
+                bool all = true;
+                for (int64_t k = 0; k < len && all; ++k)
+                    all = bd.recs[bd.by_page[bd.group_start[run[pos + k]] + t]].vis == 0xFFFFu;
+                if (all) {
+                    oc.mask_off = -1;
+                } else {
+                    oc.mask_off = int32_t(em.mask_words.size());
+                    for (int64_t k = 0; k < len; k += 2) {
+                        uint32_t w = bd.recs[bd.by_page[bd.group_start[run[pos + k]] + t]].vis;
+                        if (k + 1 < len) w |= bd.recs[bd.by_page[bd.group_start[run[pos + k + 1]] + t]].vis << 16;
+                        em.mask_words.push_back(w);
+                    }
+                }
+                em.occs.push_back(oc);
+                occ_count[rd.branch] += 1;
+            }
+            em.chunks.push_back(ch);
+            pos += len;
+        }
+    }
+
+    // partial rows: a branch read by a single occurrence writes `out` directly
+    em.branches.resize(B);
+    std::vector<std::vector<int32_t>> per_branch(B);
+    int64_t prow = 0;
+    for (size_t o = 0; o < em.occs.size(); ++o) {
+        const int32_t b = em.occs[o].branch;
+        if (occ_count[b] == 1) {
+            em.occs[o].prow_base = -1;
+        } else {
+            em.occs[o].prow_base = int32_t(prow);
+            per_branch[b].push_back(int32_t(prow));
+            prow += int64_t(in.q_off[b + 1] - in.q_off[b]) * G * Hkv;
+            if (prow > (int64_t(1) << 31) - 1) return FA_ERR_UNSUPPORTED;
+        }
+    }
+    for (int32_t b = 0; b < B; ++b) {
+        fa::Branch &br = em.branches[b];
+        std::memset(&br, 0, sizeof br);
+        br.q_begin = in.q_off[b];
+        br.n_q = in.q_off[b + 1] - in.q_off[b];
+        br.qpos0 = int32_t(in.n_b[b] - br.n_q);
+        br.merge_off = int32_t(em.merge_bases.size());
+        br.n_merge = int32_t(per_branch[b].size());
+        br.direct = occ_count[b] == 1;
+        em.merge_bases.insert(em.merge_bases.end(), per_branch[b].begin(), per_branch[b].end());
+        for (int32_t i = 0; i < br.n_q; ++i) em.q_branch.push_back(b);
+        if (occ_count[b] != 1) st.merge_rows += int64_t(br.n_q) * in.d->num_q_heads;
+    }
+
+    // work items: chunk x KV head x row group (row groups shared by every head)
+    const int32_t q_per_piece = std::max(1, fa::kRowsMax / G);
+    for (size_t c = 0; c < em.chunks.size(); ++c) {
+        const fa::Chunk &ch = em.chunks[c];
+        std::vector<std::pair<int32_t, int32_t>> groups;  // (ent_off, n_ent) with rows
+        std::vector<int32_t> group_rows;
+        int32_t cur_off = int32_t(em.ents.size()), cur_n = 0, cur_rows = 0;
+        for (int32_t t = 0; t < ch.n_occ; ++t) {
+            const int32_t o = ch.occ_off + t;
+            const int32_t nq = em.branches[em.occs[o].branch].n_q;
+            for (int32_t i0 = 0; i0 < nq; i0 += q_per_piece) {
+                const int32_t ni = std::min(q_per_piece, nq - i0);
+                if (cur_rows + ni * G > fa::kRowsMax) {
+                    groups.push_back({cur_off, cur_n});
+                    group_rows.push_back(cur_rows);
+                    cur_off = int32_t(em.ents.size());
+                    cur_n = 0;
+                    cur_rows = 0;
+                }
+                fa::Ent en;
+                std::memset(&en, 0, sizeof en);
+                en.occ = o;
+                en.i0 = i0;
+                en.ni = ni;
+                em.ents.push_back(en);
+                cur_n += 1;
+                cur_rows += ni * G;
+            }
+        }
+        if (cur_n) {
+            groups.push_back({cur_off, cur_n});
+            group_rows.push_back(cur_rows);
+        }
+        for (int32_t h = 0; h < Hkv; ++h) {
+            for (size_t gi = 0; gi < groups.size(); ++gi) {
+                fa::Item it;
+                std::memset(&it, 0, sizeof it);
+                it.chunk = int32_t(c);
+                it.head = h;
+                it.ent_off = groups[gi].first;
+                it.n_ent = groups[gi].second;
+                it.n_rows = group_rows[gi];
+                em.items_rows.push_back(it);
+                st.kv_bytes_rows += int64_t(ch.n_pages) * kPageSize * fa::kHeadDim * 2 * 2;
+            }
+        }
+    }
+
+    st.num_chunks = int64_t(em.chunks.size());
+    st.num_items_rows = int64_t(em.items_rows.size());
+    st.num_items_tensor = int64_t(em.items_tc.size());
+    st.partial_rows = prow;
+    st.total_q = in.q_off[B];
+    if (em.items_rows.size() > size_t(INT32_MAX) || em.chunk_pages.size() > size_t(INT32_MAX))
+        return FA_ERR_UNSUPPORTED;
+
+    // blob layout
+    fa::Layout &L = plan->lay;
+    std::memset(&L, 0, sizeof L);
+    int64_t off = fa::kAlign;  // error word
+    auto place = [&](int64_t bytes) { const int64_t at = off; off = align_up(off + std::max<int64_t>(bytes, 1)); return at; };
+    L.chunk_pages = place(int64_t(em.chunk_pages.size()) * 4);
+    L.chunks = place(int64_t(em.chunks.size()) * sizeof(fa::Chunk));
+    L.occs = place(int64_t(em.occs.size()) * sizeof(fa::Occ));
+    L.items_rows = place(int64_t(em.items_rows.size()) * sizeof(fa::Item));
+    L.items_tc = place(int64_t(em.items_tc.size()) * sizeof(fa::Item));
+    L.ents = place(int64_t(em.ents.size()) * sizeof(fa::Ent));
+    L.branches = place(int64_t(em.branches.size()) * sizeof(fa::Branch));
+    L.q_branch = place(int64_t(em.q_branch.size()) * 4);
+    L.merge_bases = place(int64_t(em.merge_bases.size()) * 4);
+    L.mask_words = place(int64_t(em.mask_words.size()) * 4);
+    L.total = off;
+    L.n_chunk_pages = int32_t(em.chunk_pages.size());
+    L.n_chunks = int32_t(em.chunks.size());
+    L.n_occs = int32_t(em.occs.size());
+    L.n_items_rows = int32_t(em.items_rows.size());
+    L.n_items_tc = int32_t(em.items_tc.size());
+    L.n_ents = int32_t(em.ents.size());
+    L.n_branches = B;
+    L.total_q = in.q_off[B];
+    L.n_merge_bases = int32_t(em.merge_bases.size());
+    L.n_mask_words = int32_t(em.mask_words.size());
+    plan->blob.assign(size_t(L.total), 0);
+    auto put = [&](int64_t at, const void *src, size_t bytes) { if (bytes) std::memcpy(plan->blob.data() + at, src, bytes); };
+    put(L.chunk_pages, em.chunk_pages.data(), em.chunk_pages.size() * 4);
+    put(L.chunks, em.chunks.data(), em.chunks.size() * sizeof(fa::Chunk));
+    put(L.occs, em.occs.data(), em.occs.size() * sizeof(fa::Occ));
+    put(L.items_rows, em.items_rows.data(), em.items_rows.size() * sizeof(fa::Item));
+    put(L.items_tc, em.items_tc.data(), em.items_tc.size() * sizeof(fa::Item));
+    put(L.ents, em.ents.data(), em.ents.size() * sizeof(fa::Ent));
+    put(L.branches, em.branches.data(), em.branches.size() * sizeof(fa::Branch));
+    put(L.q_branch, em.q_branch.data(), em.q_branch.size() * 4);
+    put(L.merge_bases, em.merge_bases.data(), em.merge_bases.size() * 4);
+    put(L.mask_words, em.mask_words.data(), em.mask_words.size() * 4);
+    plan->partial_rows = prow;
+    return FA_OK;
+}
+
+}  // namespace
+
+extern "C" int fork_attn_plan_create(const fa_dims *dims, const fa_desc *desc,
+                                     const fa_plan_opts *opts, fa_plan **out_plan) {
+    if (!dims || !desc || !out_plan) return FA_ERR_NULL;
+    try {
+        Input in{dims, desc, 0, {}, {}};
+        int rc = validate(in);
+        if (rc != FA_OK) return rc;
+        fa_plan_opts o;
+        std::memset(&o, 0, sizeof o);
+        if (opts) o = *opts;
+        fa_plan *p = new fa_plan();
+        p->dims = *dims;
+        p->G = in.G;
+        p->num_pages_pool = desc->num_pages_pool;
+        p->dev_plan = nullptr;
+        p->dev_scratch = nullptr;
+        p->uploaded = false;
+        rc = build_plan(in, o, p);
+        if (rc != FA_OK) {
+            delete p;
+            return rc;
+        }
+        *out_plan = p;
+        return FA_OK;
+    } catch (const std::bad_alloc &) {
+        return FA_ERR_NOMEM;
+    }
+}
+
+extern "C" int fork_attn_plan_sizes(const fa_plan *plan, size_t *plan_bytes, size_t *scratch_bytes) {
+    if (!plan || !plan_bytes || !scratch_bytes) return FA_ERR_NULL;
+    *plan_bytes = size_t(plan->lay.total);
+    *scratch_bytes = size_t(fa::scratch_bytes(plan->partial_rows));
+    return FA_OK;
+}
+
+extern "C" int fork_attn_plan_stats(const fa_plan *plan, fa_plan_stats *stats) {
+    if (!plan || !stats) return FA_ERR_NULL;
+    *stats = plan->stats;
+    return FA_OK;
+}
+
+extern "C" int fork_attn_plan_destroy(fa_plan *plan) {
+    delete plan;
+    return FA_OK;
+}
+
+extern "C" const char *fork_attn_strerror(int status) {
+    switch (status) {
+        case FA_OK: return "ok";
+        case FA_ERR_NULL: return "a required pointer is NULL";
+        case FA_ERR_INVALID: return "malformed descriptor or dimensions";
+        case FA_ERR_UNSUPPORTED: return "shape not supported (head_dim 128, page_size 16, Hq % Hkv == 0, G <= 32)";
+        case FA_ERR_RANGE: return "an index is out of range";
+        case FA_ERR_ALIGN: return "a device pointer is not suitably aligned";
+        case FA_ERR_NOT_UPLOADED: return "plan not uploaded";
+        case FA_ERR_CUDA: return "a CUDA call failed";
+        case FA_ERR_NOMEM: return "host allocation failed";
+        case FA_ERR_BUFFER_SMALL: return "a caller buffer is too small";
+        case FA_ERR_DEVICE: return "a kernel reported a device-side fault";
+        default: return "unknown status";
+    }
+}

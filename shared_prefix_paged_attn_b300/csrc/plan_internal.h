@@ -1,0 +1,33 @@
+// Host-side plan object shared by the planner (plan.cpp) and the launcher (decode.cu).
+#pragma once
+#include <stdint.h>
+
+#include <vector>
+
+#include "../../include/fork_attn.h"
+#include "plan_layout.h"
+
+struct fa_plan {
+    fa_dims dims;
+    int32_t G;                    // query heads per KV head
+    int64_t num_pages_pool;
+    fa::Layout lay;
+    std::vector<uint8_t> blob;    // host copy of the device plan buffer (lay.total bytes)
+    int64_t partial_rows;         // fp32 partial rows (each 128 floats + 1 lse)
+    fa_plan_stats stats;
+    // set by fork_attn_plan_upload
+    void *dev_plan;
+    void *dev_scratch;
+    bool uploaded;
+};
+
+namespace fa {
+inline int64_t scratch_lse_offset(int64_t partial_rows) {
+    // partial O: partial_rows x 128 fp32, then partial lse: partial_rows fp32 (256-aligned)
+    return ((partial_rows * kHeadDim * 4 + kAlign - 1) / kAlign) * kAlign;
+}
+inline int64_t scratch_bytes(int64_t partial_rows) {
+    if (partial_rows == 0) return 0;
+    return scratch_lse_offset(partial_rows) + ((partial_rows * 4 + kAlign - 1) / kAlign) * kAlign;
+}
+}  // namespace fa

@@ -1,0 +1,156 @@
+"""GPU parity: fork_attn_decode (through the C ABI) against the fp64 oracle.
+
+Tolerances (bf16 K/V and Q, fp32 accumulation): max |d out| <= 1e-2, relative L2 of out
+<= 5e-3, |d lse| <= 1e-3.  Small versions of the five workloads are checked on every output
+row; the full-size workloads (values drawn on the GPU) on sampled branches, in the launch
+configuration the benchmark uses.
+"""
+import copy
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import shared_prefix_paged_attn_b300 as fa
+from shared_prefix_paged_attn_b300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+MAX_ABS, REL_L2, LSE_ABS = 1e-2, 5e-3, 1e-3
+
+
+def gpu_decode(w, out_dtype=fa.FA_BF16, check_error=True, **opts):
+    dev = torch.device("cuda")
+    q, k, v = w.q.to(dev), w.k_pages.to(dev), w.v_pages.to(dev)
+    run = fa.ForkAttention(w, out_dtype=out_dtype, **opts)
+    out, lse = run(q, k, v)
+    torch.cuda.synchronize()
+    if check_error:
+        assert fa.fork_attn_check(run.plan) == 0
+    return out.float().cpu().numpy().reshape(-1, w.head_dim), lse.cpu().numpy().reshape(-1)
+
+
+def assert_parity(out, lse, ref_out, ref_lse, what=""):
+    empty = np.isneginf(ref_lse)
+    assert np.array_equal(np.isneginf(lse), empty), what
+    assert np.all(out[empty] == 0), what
+    fin = ~empty
+    d = np.abs(out[fin] - ref_out[fin])
+    assert d.max(initial=0.0) <= MAX_ABS, f"{what} max|d out| = {d.max()}"
+    rel = np.linalg.norm(out[fin] - ref_out[fin]) / max(np.linalg.norm(ref_out[fin]), 1e-30)
+    assert rel <= REL_L2, f"{what} rel L2 = {rel}"
+    dl = np.abs(lse[fin] - ref_lse[fin])
+    assert dl.max(initial=0.0) <= LSE_ABS, f"{what} max|d lse| = {dl.max()}"
+
+
+@pytest.mark.parametrize("cfg", [1, 2, 3, 4, 5])
+@pytest.mark.parametrize("out_dtype", [fa.FA_BF16, fa.FA_F32])
+def test_small_configs_every_row(cfg, out_dtype):
+    w = W.make(cfg, small=True)
+    out, lse = gpu_decode(w, out_dtype)
+    ref_out, ref_lse = oracle.fork_attn(w)
+    assert_parity(out, lse, ref_out, ref_lse, f"config {cfg}")
+
+
+@pytest.mark.parametrize("cfg", [1, 2, 3, 4, 5])
+def test_full_configs_sampled_branches(cfg):
+    w = W.make(cfg, device="cuda")
+    out, lse = gpu_decode(w)
+    rng = np.random.default_rng(cfg)
+    picks = sorted(set(rng.choice(w.num_branches, size=min(4, w.num_branches), replace=False).tolist())
+                   | {0, w.num_branches - 1})
+    sub = W.subset(w, picks)
+    sub.q, sub.k_pages, sub.v_pages = sub.q.cpu(), sub.k_pages.cpu(), sub.v_pages.cpu()
+    ref_out, ref_lse = oracle.fork_attn(sub)
+    rows = np.concatenate([np.arange(int(w.branch_q_off[b]) * w.num_q_heads,
+                                     int(w.branch_q_off[b + 1]) * w.num_q_heads) for b in picks])
+    assert_parity(out[rows], lse[rows], ref_out, ref_lse, f"config {cfg} full")
+
+
+@pytest.mark.parametrize("seed", range(16))
+def test_random_caches_edge_cases(seed):
+    # mid-page segment starts, shared / overlapping pages, duplicates, random drops, n_q up to 8
+    w = W.random_dag(1000 + seed, num_q_heads=8 if seed % 2 else 16, num_kv_heads=2,
+                     n_segs=6, n_branches=7, max_list=5, max_seg_len=300, pool_pages=40,
+                     drop_p=(0.0, 0.3, 0.9)[seed % 3], max_nq=8 if seed % 4 == 0 else 2)
+    out, lse = gpu_decode(w, chunk_pages=(0, 2, 5, 1)[seed % 4])
+    ref_out, ref_lse = oracle.fork_attn(w)
+    assert_parity(out, lse, ref_out, ref_lse, f"seed {seed}")
+
+
+def test_fully_masked_rows_give_zero_and_minus_infinity():
+    w = W.random_dag(7, n_branches=3, drop_p=0.0, values=True)
+    bits = [np.zeros(w.branch_len(b), bool) for b in range(w.num_branches)]
+    bits[1][:] = True
+    w.vis_bits, w.vis_word_off = W._pack_branch_bits(bits)
+    out, lse = gpu_decode(w)
+    ref_out, ref_lse = oracle.fork_attn(w)
+    assert_parity(out, lse, ref_out, ref_lse)
+    assert np.isneginf(lse).sum() > 0
+
+
+def test_single_token_and_single_page():
+    w = W.random_dag(11, n_segs=1, n_branches=1, max_seg_len=1, max_nq=1, drop_p=0.0)
+    out, lse = gpu_decode(w)
+    ref_out, ref_lse = oracle.fork_attn(w)
+    assert_parity(out, lse, ref_out, ref_lse)
+
+
+def test_run_to_run_bitwise_determinism():
+    w = W.make(5, small=True)
+    a = gpu_decode(w)
+    b = gpu_decode(w)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_page_permutation_gives_identical_output():
+    w = W.make(3, small=True)
+    base = gpu_decode(w)
+    perm = torch.randperm(w.num_pages_pool, generator=torch.Generator().manual_seed(1))
+    w2 = copy.copy(w)
+    w2.page_ids = perm.numpy()[w.page_ids].astype(np.int32)
+    w2.k_pages = torch.empty_like(w.k_pages)
+    w2.v_pages = torch.empty_like(w.v_pages)
+    w2.k_pages[perm] = w.k_pages
+    w2.v_pages[perm] = w.v_pages
+    got = gpu_decode(w2)
+    assert np.array_equal(base[0], got[0]) and np.array_equal(base[1], got[1])
+
+
+def test_garbage_in_dropped_slots_changes_nothing():
+    w = W.make(2, small=True)
+    base = gpu_decode(w)
+    seen = np.zeros(w.num_pages_pool * 16, bool)
+    for b in range(w.num_branches):
+        words = w.vis_bits[w.vis_word_off[b]:w.vis_word_off[b + 1]]
+        n = w.branch_len(b)
+        vis = (words[np.arange(n) // 32] >> (np.arange(n) % 32)) & 1
+        seen[W.logical_slots(w, b)[vis.astype(bool)]] = True
+    w2 = copy.copy(w)
+    kf = w.k_pages.clone().transpose(1, 2).reshape(-1, w.num_kv_heads, 128)
+    vf = w.v_pages.clone().transpose(1, 2).reshape(-1, w.num_kv_heads, 128)
+    hidden = torch.from_numpy(~seen)
+    kf[hidden] = 3.0e4
+    vf[hidden] = -3.0e4
+    w2.k_pages = kf.view(-1, 16, w.num_kv_heads, 128).transpose(1, 2).contiguous()
+    w2.v_pages = vf.view(-1, 16, w.num_kv_heads, 128).transpose(1, 2).contiguous()
+    got = gpu_decode(w2)
+    assert np.array_equal(base[0], got[0]) and np.array_equal(base[1], got[1])
+
+
+def test_private_pages_of_one_branch_do_not_reach_another():
+    w = W.make(1)
+    base = gpu_decode(w)
+    w2 = copy.copy(w)
+    w2.k_pages, w2.v_pages = w.k_pages.clone(), w.v_pages.clone()
+    priv = int(w.branch_segs[w.branch_seg_off[0] + 1])
+    po, tb, ln = (int(x) for x in w.segs[priv])
+    pages = torch.as_tensor(w.page_ids[po:po + (tb + ln + 15) // 16].astype(np.int64))
+    w2.k_pages[pages] = -w2.k_pages[pages]
+    w2.v_pages[pages] = 2 * w2.v_pages[pages]
+    got = gpu_decode(w2)
+    H = w.num_q_heads
+    assert not np.array_equal(base[0][:H], got[0][:H])  # branch 0 changed
+    assert np.array_equal(base[0][H:], got[0][H:])       # the others did not
+    assert np.array_equal(base[1][H:], got[1][H:])

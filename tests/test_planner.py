@@ -1,0 +1,124 @@
+"""Host planner (C++) through the C ABI, on the CPU: validation, counters, structure."""
+import ctypes
+
+import numpy as np
+import pytest
+
+import oracle
+import shared_prefix_paged_attn_b300 as fa
+from shared_prefix_paged_attn_b300 import _lib, build
+from shared_prefix_paged_attn_b300 import workloads as W
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    build.build()
+
+
+def _plan_rc(w, **kw):
+    try:
+        fa.plan_for(w, **kw)
+        return 0
+    except fa.ForkAttnError as e:
+        return e.status
+
+
+def test_unique_counters_match_the_oracle_on_all_five_configs():
+    for c in range(1, 6):
+        w = W.make(c, values=False)
+        st = fa.plan_for(w).stats()
+        slots, pages = oracle.unique_slots(w)
+        assert st["unique_visible_slots"] == slots
+        assert st["touched_pages"] == pages
+        assert st["total_q"] == w.total_q
+
+
+def test_unique_counters_on_random_caches():
+    for seed in range(20):
+        w = W.random_dag(seed, n_branches=5, n_segs=5, pool_pages=6, values=False)
+        st = fa.plan_for(w).stats()
+        assert (st["unique_visible_slots"], st["touched_pages"]) == oracle.unique_slots(w)
+
+
+def test_shared_prefix_pages_are_listed_once():
+    w = W.config1(values=False)
+    st = fa.plan_for(w).stats()
+    # 64 prefix pages + 4 x 16 private pages, each read once per KV head and row group
+    assert st["touched_pages"] == 64 + 4 * 16
+    assert st["kv_bytes_rows"] == (64 + 64) * 16 * 128 * 2 * 2 * w.num_kv_heads
+
+
+def test_fully_dropped_pages_are_skipped():
+    w = W.config4(shrink=16, values=False)
+    st = fa.plan_for(w).stats()
+    listed = sum(w.branch_len(b) for b in range(w.num_branches))
+    assert st["touched_pages"] * 16 < listed  # dropped tool segments are never read
+    assert st["kv_bytes_rows"] / (w.num_kv_heads * 512) < (w.num_pages_pool * 16) * 8
+
+
+def test_validation_errors():
+    good = W.random_dag(3, values=False)
+    assert _plan_rc(good) == 0
+
+    def variant(**kw):
+        import copy
+        v = copy.copy(good)
+        for k, val in kw.items():
+            setattr(v, k, val)
+        return v
+
+    bad_page = good.page_ids.copy(); bad_page[0] = good.num_pages_pool
+    assert _plan_rc(variant(page_ids=bad_page)) == -4
+    bad_seg = good.segs.copy(); bad_seg[0, 1] = 16
+    assert _plan_rc(variant(segs=bad_seg)) == -4
+    bad_len = good.segs.copy(); bad_len[0, 2] = 0
+    assert _plan_rc(variant(segs=bad_len)) == -2
+    past_end = good.segs.copy(); past_end[0, 0] = len(good.page_ids)
+    assert _plan_rc(variant(segs=past_end)) == -4
+    bad_list = good.branch_segs.copy(); bad_list[0] = len(good.segs)
+    assert _plan_rc(variant(branch_segs=bad_list)) == -4
+    big_q = good.branch_q_off.copy(); big_q[1:] += 10 ** 6
+    assert _plan_rc(variant(branch_q_off=big_q)) == -2
+    if good.vis_bits is not None:
+        assert _plan_rc(variant(vis_bits=good.vis_bits[:1])) == -4
+    for hq, hkv, rc in ((6, 4, -3), (64, 1, -3)):
+        assert _plan_rc(variant(num_q_heads=hq, num_kv_heads=hkv)) == rc
+
+
+def test_unsupported_dims_and_nulls():
+    w = W.config1(values=False)
+    with pytest.raises(fa.ForkAttnError) as e:
+        fa.fork_attn_plan_create(8, 2, w.page_ids, w.segs, w.branch_seg_off, w.branch_segs,
+                                 w.num_pages_pool, head_dim=64)
+    assert e.value.status == -3
+    with pytest.raises(fa.ForkAttnError) as e:
+        fa.fork_attn_plan_create(8, 2, w.page_ids, w.segs, w.branch_seg_off, w.branch_segs,
+                                 w.num_pages_pool, page_size=32)
+    assert e.value.status == -3
+    lib = _lib.load()
+    assert lib.fork_attn_plan_create(None, None, None, None) == -1
+    assert lib.fork_attn_decode(None, None, None, None, None, None, None) == -1
+
+
+def test_decode_before_upload_is_rejected():
+    w = W.config1(values=False)
+    p = fa.plan_for(w)
+    fake = ctypes.c_void_p(256)
+    rc = _lib.load().fork_attn_decode(fake, fake, fake, p.handle, fake, fake, None)
+    assert rc == -6
+
+
+def test_upload_rejects_small_or_misaligned_buffers():
+    w = W.config1(values=False)
+    p = fa.plan_for(w)
+    pb, sb = p.sizes()
+    lib = _lib.load()
+    assert lib.fork_attn_plan_upload(p.handle, ctypes.c_void_p(256), pb - 1, ctypes.c_void_p(512), sb, None) == -9
+    assert lib.fork_attn_plan_upload(p.handle, ctypes.c_void_p(260), pb, ctypes.c_void_p(512), sb, None) == -5
+    assert lib.fork_attn_plan_upload(p.handle, ctypes.c_void_p(256), pb, None, sb, None) == -1
+
+
+def test_plan_is_deterministic():
+    w = W.config3(shrink=16, values=False)
+    a, b = fa.plan_for(w), fa.plan_for(w)
+    assert a.sizes() == b.sizes() and a.stats() == b.stats()
