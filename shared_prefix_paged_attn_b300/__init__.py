@@ -130,6 +130,9 @@ def fork_attn_decode(q, k_pages, v_pages, plan: Plan, out, lse, stream=None):
 
 def fork_attn_decode_timed(q, k_pages, v_pages, plan: Plan, out, lse, events, stream=None):
     """events: 6 torch.cuda.Event(enable_timing=True), recorded around the three kernels."""
+    for e in events:  # torch creates an event's handle on its first record
+        if not e.cuda_event:
+            e.record()
     handles = (ctypes.c_void_p * 6)(*[ctypes.c_void_p(e.cuda_event) for e in events])
     _check(_lib.load().fork_attn_decode_timed(_ptr(q), _ptr(k_pages), _ptr(v_pages), plan.handle,
                                               _ptr(out), _ptr(lse), _stream_ptr(stream),

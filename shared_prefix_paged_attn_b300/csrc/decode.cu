@@ -102,8 +102,9 @@ int fill_params(const fa_plan *plan, const void *q, const void *k_pages, const v
 bool needs_merge(const fa_plan *plan) { return plan->stats.merge_rows > 0; }
 
 int launch_all(const fa::DecodeParams &p, const fa_plan *plan, cudaStream_t st, void **events) {
+    bool ev_ok = true;
     auto rec = [&](int i) {
-        if (events) cudaEventRecord(static_cast<cudaEvent_t>(events[i]), st);
+        if (events) ev_ok = ev_ok && cudaEventRecord(static_cast<cudaEvent_t>(events[i]), st) == cudaSuccess;
     };
     rec(0);
     if (p.n_items > 0)
@@ -118,7 +119,9 @@ int launch_all(const fa::DecodeParams &p, const fa_plan *plan, cudaStream_t st, 
         fa::mergek::merge_kernel<<<blocks, fa::mergek::kThreads, 0, st>>>(p);
     }
     rec(5);
-    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+    const bool launched = cudaGetLastError() == cudaSuccess;
+    if (!ev_ok) return FA_ERR_INVALID;
+    return launched ? FA_OK : FA_ERR_CUDA;
 }
 
 }  // namespace
