@@ -79,14 +79,49 @@ class ClockSampler:
 
             self._thr = threading.Thread(target=loop, daemon=True)
             self._thr.start()
-        except Exception as e:  # NVML missing: say so in the record
-            self.reasons.add(f"nvml_unavailable:{type(e).__name__}")
+        except Exception as e:  # no NVML binding: sample nvidia-smi instead
+            self.nvml_error = f"{type(e).__name__}: {e}"
+            self._start_smi()
         return self
+
+    def _start_smi(self):
+        import subprocess
+        q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
+        try:
+            self._smi = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={q}", "-i", str(self.index),
+                 "--format=csv,noheader,nounits", "-lms", "20"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception as e:
+            self.reasons.add(f"clock_sampling_unavailable:{type(e).__name__}")
+            self._smi = None
+
+    def _stop_smi(self):
+        if getattr(self, "_smi", None) is None:
+            return
+        self._smi.terminate()
+        out, _ = self._smi.communicate(timeout=10)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 6:
+                continue
+            try:
+                self.samples.append(float(f[0]))
+                self.max_mhz = float(f[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[2:6]):
+                if v.lower() in ("active", "1", "yes"):
+                    self.reasons.add(n)
 
     def __exit__(self, *a):
         self._stop.set()
         if self._thr:
             self._thr.join()
+        self._stop_smi()
 
     def record(self):
         return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
@@ -307,7 +342,7 @@ def run_ours(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", type=int, default=4)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
