@@ -61,7 +61,9 @@ enum {
     FA_ERR_CUDA = -7,          /* a CUDA runtime / driver call failed                         */
     FA_ERR_NOMEM = -8,         /* host allocation failed                                      */
     FA_ERR_BUFFER_SMALL = -9,  /* a caller buffer is smaller than fork_attn_plan_sizes says   */
-    FA_ERR_DEVICE = -10        /* a kernel reported a fault through the plan's error word     */
+    FA_ERR_DEVICE = -10,       /* a kernel reported a fault through the plan's error word     */
+    FA_ERR_SCRATCH_LIMIT = -11 /* the plan needs more than fork_attn_decode_static_scratch's  */
+                               /* built-in device array holds (FA_STATIC_SCRATCH_BYTES)        */
 };
 
 enum { FA_BF16 = 0, FA_F32 = 1 };
@@ -189,6 +191,37 @@ int fork_attn_decode_timed(const void *q, const void *k_pages, const void *v_pag
  * and clears it.  A non-zero word means a kernel gave up (an expired wait or a failed check)
  * and the outputs of that decode are not valid. */
 int fork_attn_check(fa_plan *plan, int32_t *device_error, void *stream);
+
+/* Size of the device array used by fork_attn_decode_static_scratch: 32 MiB. */
+#define FA_STATIC_SCRATCH_BYTES (32u << 20)
+
+/* A decode for callers that cannot allocate device memory at all: an engine plugin whose
+ * host owns every device allocation and hands it only the input and output tensors, or code
+ * that must not touch the allocator while it runs (a latency-critical loop, or a region
+ * where the allocator is locked).  The source pages have no counterpart of this call; it
+ * exists only so that such callers can run the same plan.
+ *
+ * The caller passes the same inputs and outputs as to fork_attn_decode and a plan from
+ * fork_attn_plan_create; the plan does not need fork_attn_plan_upload.  Instead of caller
+ * buffers, the plan arrays and the fp32 partial results live in one device array of
+ * FA_STATIC_SCRATCH_BYTES that the library defines at file scope: every GPU that loads the
+ * library holds it until the process exits.  Each call copies the plan arrays into the array
+ * (cudaMemcpyAsync from host memory, on `stream`; this also clears the device error word)
+ * and then runs the same kernels as fork_attn_decode.  Nothing is allocated: no cudaMalloc,
+ * no cudaFree, no allocating library routine.
+ *
+ * The first call on a device (made current by the caller) looks up the array's device
+ * address with cudaGetSymbolAddress; make that first call before any stream capture.
+ * Every call on a device shares the one array and leaves the last call's contents in it:
+ * two calls whose work overlaps on the GPU (different streams, or different host threads)
+ * race on it, so serialise them.  The device error word of these calls is not readable
+ * through fork_attn_check.
+ *
+ * Errors: FA_ERR_NULL, FA_ERR_ALIGN (as fork_attn_decode), FA_ERR_SCRATCH_LIMIT when
+ * plan_bytes + scratch_bytes of fork_attn_plan_sizes exceed FA_STATIC_SCRATCH_BYTES (checked
+ * before any CUDA call), FA_ERR_CUDA. */
+int fork_attn_decode_static_scratch(const void *q, const void *k_pages, const void *v_pages,
+                                    const fa_plan *plan, void *out, float *lse, void *stream);
 
 /* Frees the host plan.  Device buffers stay owned by the caller. */
 int fork_attn_plan_destroy(fa_plan *plan);

@@ -14,7 +14,7 @@ from . import _lib
 from ._lib import FA_BF16, FA_F32, FaDesc, FaDims, FaPlanOpts, FaPlanStats
 
 __all__ = ["ForkAttnError", "Plan", "fork_attn_plan_create", "fork_attn_decode",
-           "fork_attn_decode_timed", "fork_attn_check", "fork_attn_strerror", "FA_BF16",
+           "fork_attn_decode_timed", "fork_attn_decode_static_scratch", "fork_attn_check", "fork_attn_strerror", "FA_BF16",
            "FA_F32", "plan_for", "ForkAttention"]
 
 
@@ -137,6 +137,15 @@ def fork_attn_decode_timed(q, k_pages, v_pages, plan: Plan, out, lse, events, st
     _check(_lib.load().fork_attn_decode_timed(_ptr(q), _ptr(k_pages), _ptr(v_pages), plan.handle,
                                               _ptr(out), _ptr(lse), _stream_ptr(stream),
                                               handles, 3), "fork_attn_decode_timed")
+
+
+def fork_attn_decode_static_scratch(q, k_pages, v_pages, plan: Plan, out, lse, stream=None):
+    """Decode with the library's built-in device array for plan arrays and partials (for
+    callers that cannot allocate device memory); the plan needs no upload."""
+    _check(_lib.load().fork_attn_decode_static_scratch(_ptr(q), _ptr(k_pages), _ptr(v_pages),
+                                                       plan.handle, _ptr(out), _ptr(lse),
+                                                       _stream_ptr(stream)),
+           "fork_attn_decode_static_scratch")
 
 
 def fork_attn_check(plan: Plan, stream=None) -> int:

@@ -8,6 +8,7 @@ LIB_PATH = os.path.join(HERE, "libforkattn.so")
 c_int32, c_int64, c_float, c_void_p = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p
 
 FA_OK = 0
+FA_STATIC_SCRATCH_BYTES = 32 << 20
 FA_BF16, FA_F32 = 0, 1
 
 
@@ -59,6 +60,8 @@ SIGNATURES = {
     "fork_attn_decode_timed": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                          c_void_p, c_void_p, ctypes.POINTER(c_void_p), c_int32]),
     "fork_attn_check": (c_int32, [c_void_p, ctypes.POINTER(c_int32), c_void_p]),
+    "fork_attn_decode_static_scratch": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p,
+                                                  c_void_p, c_void_p, c_void_p]),
     "fork_attn_plan_destroy": (c_int32, [c_void_p]),
     "fork_attn_strerror": (ctypes.c_char_p, [c_int32]),
 }

@@ -184,3 +184,69 @@ extern "C" int fork_attn_check(fa_plan *plan, int32_t *device_error, void *strea
     }
     return FA_OK;
 }
+
+// ---------------------------------------------------------------------------------------
+// Decode without caller-provided device buffers beyond inputs and outputs.
+//
+// For callers that cannot allocate device memory (see fork_attn_decode_static_scratch in
+// fork_attn.h): the plan arrays and the fp32 partials live in one file-scope device array.
+// Nothing here allocates.  The array is shared by every call on a device; calls that overlap
+// on the GPU race on it.
+namespace {
+
+constexpr size_t kStaticScratchBytes = FA_STATIC_SCRATCH_BYTES;
+static_assert(kStaticScratchBytes % fa::kAlign == 0, "whole alignment units");
+__device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
+
+// Device address of g_static_scratch on the current device, looked up once per device with
+// that device current (the host-side name of the array is not a device address).
+uint8_t *static_scratch_address() {
+    static std::mutex mu;
+    static uint8_t *addr[128] = {nullptr};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return nullptr;
+    std::lock_guard<std::mutex> lk(mu);
+    if (!addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess) return nullptr;
+        addr[dev] = static_cast<uint8_t *>(p);
+    }
+    return addr[dev];
+}
+
+}  // namespace
+
+extern "C" int fork_attn_decode_static_scratch(const void *q, const void *k_pages, const void *v_pages,
+                                               const fa_plan *plan, void *out, float *lse, void *stream) {
+    if (!plan || !q || !k_pages || !v_pages || !out || !lse) return FA_ERR_NULL;
+    if (!aligned(q, 16) || !aligned(k_pages, 16) || !aligned(v_pages, 16) || !aligned(out, 16) ||
+        !aligned(lse, 16))
+        return FA_ERR_ALIGN;
+    const size_t plan_bytes = size_t(plan->lay.total);  // a multiple of 256
+    const size_t scratch = size_t(fa::scratch_bytes(plan->partial_rows));
+    if (plan_bytes + scratch > kStaticScratchBytes) return FA_ERR_SCRATCH_LIMIT;
+    int rc = set_smem_attr();
+    if (rc != FA_OK) return rc;
+    uint8_t *base = static_scratch_address();
+    if (!base) return FA_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // the copy brings the plan arrays and a zero error word; partial rows need no clearing
+    // because every one of them is written before the merge reads it
+    if (cudaMemcpyAsync(base, plan->blob.data(), plan_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
+        return FA_ERR_CUDA;
+    fa::DecodeParams p;
+    rc = fill_params(plan, q, k_pages, v_pages, out, lse, scratch ? base + plan_bytes : nullptr, p);
+    if (rc != FA_OK) return rc;
+    const fa::Layout &L = plan->lay;
+    p.chunk_pages = reinterpret_cast<const int32_t *>(base + L.chunk_pages);
+    p.chunks = reinterpret_cast<const fa::Chunk *>(base + L.chunks);
+    p.occs = reinterpret_cast<const fa::Occ *>(base + L.occs);
+    p.items = reinterpret_cast<const fa::Item *>(base + L.items_rows);
+    p.ents = reinterpret_cast<const fa::Ent *>(base + L.ents);
+    p.branches = reinterpret_cast<const fa::Branch *>(base + L.branches);
+    p.q_branch = reinterpret_cast<const int32_t *>(base + L.q_branch);
+    p.merge_bases = reinterpret_cast<const int32_t *>(base + L.merge_bases);
+    p.mask_words = reinterpret_cast<const uint32_t *>(base + L.mask_words);
+    p.err = reinterpret_cast<int32_t *>(base);
+    return launch_all(p, plan, st, nullptr);
+}

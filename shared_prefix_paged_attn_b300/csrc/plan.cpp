@@ -485,6 +485,7 @@ extern "C" const char *fork_attn_strerror(int status) {
         case FA_ERR_NOMEM: return "host allocation failed";
         case FA_ERR_BUFFER_SMALL: return "a caller buffer is too small";
         case FA_ERR_DEVICE: return "a kernel reported a device-side fault";
+        case FA_ERR_SCRATCH_LIMIT: return "plan needs more device memory than the built-in static scratch array holds";
         default: return "unknown status";
     }
 }
