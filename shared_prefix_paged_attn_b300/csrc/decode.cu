@@ -8,6 +8,7 @@
 #include "merge_kernel.cuh"
 #include "plan_internal.h"
 #include "row_kernel.cuh"
+#include "tc_kernel.cuh"
 
 namespace {
 
@@ -57,7 +58,9 @@ int set_smem_attr() {
     std::lock_guard<std::mutex> lk(mu);
     if (!done[dev]) {
         if (cudaFuncSetAttribute(fa::rowk::row_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 int(fa::rowk::kSmemBytes)) != cudaSuccess)
+                                 int(fa::rowk::kSmemBytes)) != cudaSuccess ||
+            cudaFuncSetAttribute(fa::tck::tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(fa::tck::kSmemBytes)) != cudaSuccess)
             return FA_ERR_CUDA;
         done[dev] = true;
     }
@@ -83,6 +86,7 @@ int fill_params(const fa_plan *plan, const void *q, const void *k_pages, const v
     p.chunks = reinterpret_cast<const fa::Chunk *>(base + L.chunks);
     p.occs = reinterpret_cast<const fa::Occ *>(base + L.occs);
     p.items = reinterpret_cast<const fa::Item *>(base + L.items_rows);
+    p.items_tc = reinterpret_cast<const fa::Item *>(base + L.items_tc);
     p.ents = reinterpret_cast<const fa::Ent *>(base + L.ents);
     p.branches = reinterpret_cast<const fa::Branch *>(base + L.branches);
     p.q_branch = reinterpret_cast<const int32_t *>(base + L.q_branch);
@@ -95,6 +99,8 @@ int fill_params(const fa_plan *plan, const void *q, const void *k_pages, const v
     p.out_dtype = plan->dims.out_dtype;
     p.scale_log2 = plan->dims.scale * 1.4426950408889634f;
     p.n_items = L.n_items_rows;
+    p.n_items_tc = L.n_items_tc;
+    p.pool_pages = int32_t(plan->num_pages_pool);
     p.total_rows = L.total_q * plan->dims.num_q_heads;
     return FA_OK;
 }
@@ -110,7 +116,9 @@ int launch_all(const fa::DecodeParams &p, const fa_plan *plan, cudaStream_t st, 
     if (p.n_items > 0)
         fa::rowk::row_kernel<<<p.n_items, fa::rowk::kThreads, fa::rowk::kSmemBytes, st>>>(p);
     rec(1);
-    rec(2);  // tcgen05 kernel slot (no items in this plan)
+    rec(2);
+    if (p.n_items_tc > 0)
+        fa::tck::tc_kernel<<<p.n_items_tc, fa::tck::kThreads, fa::tck::kSmemBytes, st>>>(p);
     rec(3);
     rec(4);
     if (needs_merge(plan)) {
@@ -242,6 +250,7 @@ extern "C" int fork_attn_decode_static_scratch(const void *q, const void *k_page
     p.chunks = reinterpret_cast<const fa::Chunk *>(base + L.chunks);
     p.occs = reinterpret_cast<const fa::Occ *>(base + L.occs);
     p.items = reinterpret_cast<const fa::Item *>(base + L.items_rows);
+    p.items_tc = reinterpret_cast<const fa::Item *>(base + L.items_tc);
     p.ents = reinterpret_cast<const fa::Ent *>(base + L.ents);
     p.branches = reinterpret_cast<const fa::Branch *>(base + L.branches);
     p.q_branch = reinterpret_cast<const int32_t *>(base + L.q_branch);

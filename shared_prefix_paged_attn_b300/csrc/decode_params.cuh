@@ -19,7 +19,8 @@ struct DecodeParams {
     const int32_t *chunk_pages;
     const Chunk *chunks;
     const Occ *occs;
-    const Item *items;
+    const Item *items;     // row-kernel work items
+    const Item *items_tc;  // tcgen05-kernel work items
     const Ent *ents;
     const Branch *branches;
     const int32_t *q_branch;
@@ -29,6 +30,8 @@ struct DecodeParams {
     int32_t Hq, Hkv, G, out_dtype;
     float scale_log2;  // scale * log2(e): scores are kept in base 2 inside the kernels
     int32_t n_items;
+    int32_t n_items_tc;
+    int32_t pool_pages;  // page index one past the pool: TMA reads it as zeros
     int32_t total_rows;  // total_q * Hq
 };
 

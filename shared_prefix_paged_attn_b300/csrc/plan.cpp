@@ -236,6 +236,8 @@ int build_plan(Input &in, const fa_plan_opts &opts, fa_plan *plan) {
     fa_plan_stats &st = plan->stats;
     std::memset(&st, 0, sizeof st);
 
+    const int32_t tmin = opts.tensor_min_rows < 0 ? 0 : (opts.tensor_min_rows > 0 ? opts.tensor_min_rows : 64);
+    std::vector<char> chunk_tc;  // per chunk: its items go to the tcgen05 kernel
     std::vector<int32_t> occ_count(B, 0);
     for (const auto &run : runs) {
         const int32_t g0 = run[0];
@@ -250,11 +252,14 @@ int build_plan(Input &in, const fa_plan_opts &opts, fa_plan *plan) {
         int64_t target = std::max<int64_t>(base_pages, 2 * rows);
         if (opts.chunk_pages > 0) target = opts.chunk_pages;
         target = std::min<int64_t>(target, 256);
+        const bool tc_run = tmin > 0 && rows >= tmin;
         const int64_t n = int64_t(run.size());
         const int64_t n_ch = std::max<int64_t>(1, ceil_div(n, target));
+        // tcgen05 chunks are whole 128-token tiles (8 pages) except the last one of a run
+        const int64_t tc_len = ceil_div(ceil_div(n, n_ch), 8) * 8;
         int64_t pos = 0;
-        for (int64_t c = 0; c < n_ch; ++c) {
-            const int64_t len = n / n_ch + (c < n % n_ch ? 1 : 0);
+        for (int64_t c = 0; pos < n; ++c) {
+            const int64_t len = tc_run ? std::min(tc_len, n - pos) : n / n_ch + (c < n % n_ch ? 1 : 0);
             fa::Chunk ch;
             ch.page_off = int32_t(em.chunk_pages.size());
             ch.n_pages = int32_t(len);
@@ -264,7 +269,7 @@ int build_plan(Input &in, const fa_plan_opts &opts, fa_plan *plan) {
                 const int32_t g = run[pos + k];
                 em.chunk_pages.push_back(bd.recs[bd.by_page[bd.group_start[g]]].page);
                 st.unique_visible_slots += __builtin_popcount(bd.group_union[g]);
-                st.unique_slots_rows += __builtin_popcount(bd.group_union[g]);
+                (tc_run ? st.unique_slots_tensor : st.unique_slots_rows) += __builtin_popcount(bd.group_union[g]);
                 st.touched_pages += 1;
                 for (int32_t t = 0; t < n_read; ++t)
                     st.listed_visible_slots += __builtin_popcount(bd.recs[bd.by_page[bd.group_start[g] + t]].vis);
@@ -292,6 +297,7 @@ int build_plan(Input &in, const fa_plan_opts &opts, fa_plan *plan) {
                 occ_count[rd.branch] += 1;
             }
             em.chunks.push_back(ch);
+            chunk_tc.push_back(tc_run ? 1 : 0);
             pos += len;
         }
     }
@@ -325,10 +331,13 @@ int build_plan(Input &in, const fa_plan_opts &opts, fa_plan *plan) {
         if (occ_count[b] != 1) st.merge_rows += int64_t(br.n_q) * in.d->num_q_heads;
     }
 
-    // work items: chunk x KV head x row group (row groups shared by every head)
-    const int32_t q_per_piece = std::max(1, fa::kRowsMax / G);
+    // work items: chunk x KV head x row group (row groups shared by every head); row groups
+    // hold <= 32 rows for the row kernel and <= 256 rows (two M = 128 tiles) for tcgen05
     for (size_t c = 0; c < em.chunks.size(); ++c) {
         const fa::Chunk &ch = em.chunks[c];
+        const bool tc = chunk_tc[c] != 0;
+        const int32_t max_rows = tc ? 2 * fa::kTcRows : fa::kRowsMax;
+        const int32_t q_per_piece = std::max(1, max_rows / G);
         std::vector<std::pair<int32_t, int32_t>> groups;  // (ent_off, n_ent) with rows
         std::vector<int32_t> group_rows;
         int32_t cur_off = int32_t(em.ents.size()), cur_n = 0, cur_rows = 0;
@@ -337,7 +346,7 @@ int build_plan(Input &in, const fa_plan_opts &opts, fa_plan *plan) {
             const int32_t nq = em.branches[em.occs[o].branch].n_q;
             for (int32_t i0 = 0; i0 < nq; i0 += q_per_piece) {
                 const int32_t ni = std::min(q_per_piece, nq - i0);
-                if (cur_rows + ni * G > fa::kRowsMax) {
+                if (cur_rows + ni * G > max_rows) {
                     groups.push_back({cur_off, cur_n});
                     group_rows.push_back(cur_rows);
                     cur_off = int32_t(em.ents.size());
@@ -367,8 +376,14 @@ int build_plan(Input &in, const fa_plan_opts &opts, fa_plan *plan) {
                 it.ent_off = groups[gi].first;
                 it.n_ent = groups[gi].second;
                 it.n_rows = group_rows[gi];
-                em.items_rows.push_back(it);
-                st.kv_bytes_rows += int64_t(ch.n_pages) * kPageSize * fa::kHeadDim * 2 * 2;
+                const int64_t kv = int64_t(ch.n_pages) * kPageSize * fa::kHeadDim * 2 * 2;
+                if (tc) {
+                    em.items_tc.push_back(it);
+                    st.kv_bytes_tensor += kv;
+                } else {
+                    em.items_rows.push_back(it);
+                    st.kv_bytes_rows += kv;
+                }
             }
         }
     }
@@ -378,7 +393,8 @@ int build_plan(Input &in, const fa_plan_opts &opts, fa_plan *plan) {
     st.num_items_tensor = int64_t(em.items_tc.size());
     st.partial_rows = prow;
     st.total_q = in.q_off[B];
-    if (em.items_rows.size() > size_t(INT32_MAX) || em.chunk_pages.size() > size_t(INT32_MAX))
+    if (em.items_rows.size() > size_t(INT32_MAX) || em.items_tc.size() > size_t(INT32_MAX) ||
+        em.chunk_pages.size() > size_t(INT32_MAX))
         return FA_ERR_UNSUPPORTED;
 
     // blob layout

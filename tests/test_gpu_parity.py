@@ -154,3 +154,25 @@ def test_private_pages_of_one_branch_do_not_reach_another():
     assert not np.array_equal(base[0][:H], got[0][:H])  # branch 0 changed
     assert np.array_equal(base[0][H:], got[0][H:])       # the others did not
     assert np.array_equal(base[1][H:], got[1][H:])
+
+
+@pytest.mark.parametrize("seed", range(16))
+def test_random_caches_all_on_tensor_cores(seed):
+    # every run, however few readers it has, goes to the tcgen05 kernel: mid-page starts,
+    # ragged chunk tails, duplicates, causal multi-token rows and drops on the M = 128 tiles
+    w = W.random_dag(2000 + seed, num_q_heads=8 if seed % 2 else 16, num_kv_heads=2,
+                     n_segs=6, n_branches=7, max_list=5, max_seg_len=300, pool_pages=40,
+                     drop_p=(0.0, 0.3, 0.9)[seed % 3], max_nq=8 if seed % 4 == 0 else 2)
+    out, lse = gpu_decode(w, chunk_pages=(0, 2, 9, 24)[seed % 4], tensor_min_rows=1)
+    ref_out, ref_lse = oracle.fork_attn(w)
+    assert_parity(out, lse, ref_out, ref_lse, f"seed {seed}")
+
+
+@pytest.mark.parametrize("cfg", [2, 3, 4, 5])
+@pytest.mark.parametrize("tmin", [-1, 1])
+def test_small_configs_kernel_split(cfg, tmin):
+    # -1: everything on the row kernel; 1: everything on the tcgen05 kernel
+    w = W.make(cfg, small=True)
+    out, lse = gpu_decode(w, fa.FA_F32, tensor_min_rows=tmin)
+    ref_out, ref_lse = oracle.fork_attn(w)
+    assert_parity(out, lse, ref_out, ref_lse, f"config {cfg} tmin {tmin}")
