@@ -47,6 +47,23 @@ bool encode_pages(CUtensorMap *map, const void *pages, int64_t pool, int32_t hkv
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// V pages seen as a 5-D tensor (64 dims, 16 tokens, 2 dim-halves, Hkv, pool) so that one box
+// of 64 x 16 x 2 lands a whole page-head (4 KiB) in shared memory as [half][token][64 dims],
+// 128-byte swizzled: half the requests of two 64 x 16 boxes.
+bool encode_pages_whole(CUtensorMap *map, const void *pages, int64_t pool, int32_t hkv) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[5] = {64, cuuint64_t(fa::kPageSize), 2, cuuint64_t(hkv), cuuint64_t(pool)};
+    const cuuint64_t strides[4] = {cuuint64_t(fa::kHeadDim * 2), 128,
+                                   cuuint64_t(fa::kPageSize * fa::kHeadDim * 2),
+                                   cuuint64_t(hkv) * fa::kPageSize * fa::kHeadDim * 2};
+    const cuuint32_t box[5] = {64, cuuint32_t(fa::kPageSize), 2, 1, 1};
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(pages), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 int set_smem_attr() {
@@ -62,6 +79,13 @@ int set_smem_attr() {
             cudaFuncSetAttribute(fa::tck::tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  int(fa::tck::kSmemBytes)) != cudaSuccess)
             return FA_ERR_CUDA;
+        // the tcgen05 kernel re-splits its registers with setmaxnreg; the split must fit in
+        // what the block is launched with, or the increase would wait forever
+        cudaFuncAttributes fattr;
+        if (cudaFuncGetAttributes(&fattr, fa::tck::tc_kernel) != cudaSuccess) return FA_ERR_CUDA;
+        if (int64_t(fattr.numRegs) * fa::tck::kThreads <
+            128 * int64_t(fa::tck::kLowRegs) + 256 * int64_t(fa::tck::kHighRegs))
+            return FA_ERR_UNSUPPORTED;
         done[dev] = true;
     }
     return FA_OK;
@@ -71,7 +95,8 @@ int fill_params(const fa_plan *plan, const void *q, const void *k_pages, const v
                 float *lse, void *scratch, fa::DecodeParams &p) {
     std::memset(&p, 0, sizeof p);
     if (!encode_pages(&p.kmap, k_pages, plan->num_pages_pool, plan->dims.num_kv_heads) ||
-        !encode_pages(&p.vmap, v_pages, plan->num_pages_pool, plan->dims.num_kv_heads))
+        !encode_pages(&p.vmap, v_pages, plan->num_pages_pool, plan->dims.num_kv_heads) ||
+        !encode_pages_whole(&p.vmap_page, v_pages, plan->num_pages_pool, plan->dims.num_kv_heads))
         return FA_ERR_CUDA;
     const fa::Layout &L = plan->lay;
     uint8_t *base = static_cast<uint8_t *>(plan->dev_plan);
@@ -84,10 +109,9 @@ int fill_params(const fa_plan *plan, const void *q, const void *k_pages, const v
                          : nullptr;
     p.chunk_pages = reinterpret_cast<const int32_t *>(base + L.chunk_pages);
     p.chunks = reinterpret_cast<const fa::Chunk *>(base + L.chunks);
-    p.occs = reinterpret_cast<const fa::Occ *>(base + L.occs);
     p.items = reinterpret_cast<const fa::Item *>(base + L.items_rows);
     p.items_tc = reinterpret_cast<const fa::Item *>(base + L.items_tc);
-    p.ents = reinterpret_cast<const fa::Ent *>(base + L.ents);
+    p.rows = reinterpret_cast<const fa::RowRec *>(base + L.rows);
     p.branches = reinterpret_cast<const fa::Branch *>(base + L.branches);
     p.q_branch = reinterpret_cast<const int32_t *>(base + L.q_branch);
     p.merge_bases = reinterpret_cast<const int32_t *>(base + L.merge_bases);
@@ -248,10 +272,9 @@ extern "C" int fork_attn_decode_static_scratch(const void *q, const void *k_page
     const fa::Layout &L = plan->lay;
     p.chunk_pages = reinterpret_cast<const int32_t *>(base + L.chunk_pages);
     p.chunks = reinterpret_cast<const fa::Chunk *>(base + L.chunks);
-    p.occs = reinterpret_cast<const fa::Occ *>(base + L.occs);
     p.items = reinterpret_cast<const fa::Item *>(base + L.items_rows);
     p.items_tc = reinterpret_cast<const fa::Item *>(base + L.items_tc);
-    p.ents = reinterpret_cast<const fa::Ent *>(base + L.ents);
+    p.rows = reinterpret_cast<const fa::RowRec *>(base + L.rows);
     p.branches = reinterpret_cast<const fa::Branch *>(base + L.branches);
     p.q_branch = reinterpret_cast<const int32_t *>(base + L.q_branch);
     p.merge_bases = reinterpret_cast<const int32_t *>(base + L.merge_bases);

@@ -11,6 +11,7 @@ namespace fa {
 struct DecodeParams {
     CUtensorMap kmap;  // K pages viewed as [pages][Hkv][16][128] bf16, box 64 x 16, 128B swizzle
     CUtensorMap vmap;  // same for V
+    CUtensorMap vmap_page;  // V as [pages][Hkv][2 halves][16][64]: one box = a whole page-head
     const __nv_bfloat16 *q;
     void *out;
     float *lse;
@@ -18,10 +19,9 @@ struct DecodeParams {
     float *part_lse;  // [partial_rows] fp32, natural log
     const int32_t *chunk_pages;
     const Chunk *chunks;
-    const Occ *occs;
     const Item *items;     // row-kernel work items
     const Item *items_tc;  // tcgen05-kernel work items
-    const Ent *ents;
+    const RowRec *rows;
     const Branch *branches;
     const int32_t *q_branch;
     const int32_t *merge_bases;

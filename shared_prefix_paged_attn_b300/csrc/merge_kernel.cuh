@@ -5,8 +5,9 @@
 // branch's results are merged.  For a (query token, query head) row with partials
 // (O_k, lse_k) over disjoint sets of entries:
 //     L = max_k lse_k + ln sum_k exp(lse_k - max_k lse_k),    O = sum_k exp(lse_k - L) O_k.
-// One warp per row; each lane owns 4 of the 128 dims; partials are visited in the plan's
-// fixed order, so the result is bitwise run-to-run deterministic.
+// One warp per row; each lane owns 4 of the 128 dims.  The partials' lse values are spread
+// over the lanes (max and weights by shuffles); the O terms are summed in the plan's fixed
+// order, four loads in flight at a time, so the result is bitwise run-to-run deterministic.
 #pragma once
 #include "decode_params.cuh"
 #include "ptx.cuh"
@@ -24,18 +25,56 @@ __global__ void __launch_bounds__(kThreads) merge_kernel(const __grid_constant__
     const Branch br = p.branches[p.q_branch[qt]];
     if (br.direct) return;  // its only chunk wrote the output
     const int i = qt - br.q_begin, g = h / p.G, jh = h % p.G;
-    const int off = g * (br.n_q * p.G) + i * p.G + jh;
+    const int off = (i * p.G + jh) * p.Hkv + g;
+    const int32_t *bases = p.merge_bases + br.merge_off;
+    const int n = br.n_merge;
+
+    // partial k's lse sits in lane k % 32 (rounds of 32); max and weights by shuffles
     float M = -INFINITY;
-    for (int k = 0; k < br.n_merge; ++k) M = fmaxf(M, p.part_lse[p.merge_bases[br.merge_off + k] + off]);
+    for (int k0 = 0; k0 < n; k0 += 32)
+        if (k0 + lane < n) M = fmaxf(M, p.part_lse[bases[k0 + lane] + off]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     float L = 0.f;
     if (M != -INFINITY) {
-        for (int k = 0; k < br.n_merge; ++k) {
-            const int prow = p.merge_bases[br.merge_off + k] + off;
-            const float w = expf(p.part_lse[prow] - M);
-            const float4 v = *reinterpret_cast<const float4 *>(p.part_o + size_t(prow) * kHeadDim + lane * 4);
-            L += w;
-            acc.x += w * v.x; acc.y += w * v.y; acc.z += w * v.z; acc.w += w * v.w;
+        for (int k0 = 0; k0 < n; k0 += 32) {
+            const int kn = min(32, n - k0);
+            float wl = 0.f;
+            int pr = 0;
+            if (lane < kn) {
+                pr = bases[k0 + lane] + off;
+                wl = expf(p.part_lse[pr] - M);
+            }
+            // L in a fixed order: lane sums are added serially below, like the O terms
+            int k = 0;
+            for (; k + 4 <= kn; k += 4) {
+                float w[4];
+                int r[4];
+                float4 v[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    w[u] = __shfl_sync(0xffffffffu, wl, k + u);
+                    r[u] = __shfl_sync(0xffffffffu, pr, k + u);
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    v[u] = *reinterpret_cast<const float4 *>(p.part_o + size_t(r[u]) * kHeadDim + lane * 4);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    L += w[u];
+                    acc.x += w[u] * v[u].x; acc.y += w[u] * v[u].y;
+                    acc.z += w[u] * v[u].z; acc.w += w[u] * v[u].w;
+                }
+            }
+            for (; k < kn; ++k) {
+                const float w = __shfl_sync(0xffffffffu, wl, k);
+                const int r = __shfl_sync(0xffffffffu, pr, k);
+                const float4 v = *reinterpret_cast<const float4 *>(p.part_o + size_t(r) * kHeadDim + lane * 4);
+                L += w;
+                acc.x += w * v.x; acc.y += w * v.y; acc.z += w * v.z; acc.w += w * v.w;
+            }
         }
         const float inv = 1.f / L;
         acc.x *= inv; acc.y *= inv; acc.z *= inv; acc.w *= inv;

@@ -217,7 +217,7 @@ struct Emit {
     std::vector<fa::Chunk> chunks;
     std::vector<fa::Occ> occs;
     std::vector<fa::Item> items_rows, items_tc;
-    std::vector<fa::Ent> ents;
+    std::vector<fa::RowRec> rows;
     std::vector<fa::Branch> branches;
     std::vector<int32_t> q_branch, merge_bases;
     std::vector<uint32_t> mask_words;
@@ -251,7 +251,7 @@ int build_plan(Input &in, const fa_plan_opts &opts, fa_plan *plan) {
         // n pages carries n * 8 KiB of K+V, so n >= 2 * rows keeps partials near 6% of KV.
         int64_t target = std::max<int64_t>(base_pages, 2 * rows);
         if (opts.chunk_pages > 0) target = opts.chunk_pages;
-        target = std::min<int64_t>(target, 256);
+        target = std::min<int64_t>(target, fa::kMaxChunkPages);
         const bool tc_run = tmin > 0 && rows >= tmin;
         const int64_t n = int64_t(run.size());
         const int64_t n_ch = std::max<int64_t>(1, ceil_div(n, target));
@@ -333,49 +333,45 @@ int build_plan(Input &in, const fa_plan_opts &opts, fa_plan *plan) {
 
     // work items: chunk x KV head x row group (row groups shared by every head); row groups
     // hold <= 32 rows for the row kernel and <= 256 rows (two M = 128 tiles) for tcgen05
+    const int32_t Hq = in.d->num_q_heads;
     for (size_t c = 0; c < em.chunks.size(); ++c) {
         const fa::Chunk &ch = em.chunks[c];
         const bool tc = chunk_tc[c] != 0;
         const int32_t max_rows = tc ? 2 * fa::kTcRows : fa::kRowsMax;
         const int32_t q_per_piece = std::max(1, max_rows / G);
-        std::vector<std::pair<int32_t, int32_t>> groups;  // (ent_off, n_ent) with rows
-        std::vector<int32_t> group_rows;
-        int32_t cur_off = int32_t(em.ents.size()), cur_n = 0, cur_rows = 0;
+        std::vector<std::pair<int32_t, int32_t>> groups;  // (row_off, n_rows)
+        int32_t cur_off = int32_t(em.rows.size()), cur_rows = 0;
         for (int32_t t = 0; t < ch.n_occ; ++t) {
-            const int32_t o = ch.occ_off + t;
-            const int32_t nq = em.branches[em.occs[o].branch].n_q;
-            for (int32_t i0 = 0; i0 < nq; i0 += q_per_piece) {
-                const int32_t ni = std::min(q_per_piece, nq - i0);
+            const fa::Occ &oc = em.occs[ch.occ_off + t];
+            const fa::Branch &br = em.branches[oc.branch];
+            for (int32_t i0 = 0; i0 < br.n_q; i0 += q_per_piece) {
+                const int32_t ni = std::min(q_per_piece, br.n_q - i0);
                 if (cur_rows + ni * G > max_rows) {
-                    groups.push_back({cur_off, cur_n});
-                    group_rows.push_back(cur_rows);
-                    cur_off = int32_t(em.ents.size());
-                    cur_n = 0;
+                    groups.push_back({cur_off, cur_rows});
+                    cur_off = int32_t(em.rows.size());
                     cur_rows = 0;
                 }
-                fa::Ent en;
-                std::memset(&en, 0, sizeof en);
-                en.occ = o;
-                en.i0 = i0;
-                en.ni = ni;
-                em.ents.push_back(en);
-                cur_n += 1;
+                for (int32_t i = i0; i < i0 + ni; ++i)
+                    for (int32_t jh = 0; jh < G; ++jh) {
+                        fa::RowRec r;
+                        r.qrow0 = (br.q_begin + i) * Hq + jh;
+                        r.climit = br.qpos0 + i - oc.lpos0;
+                        r.mask_off = oc.mask_off;
+                        r.prow0 = oc.prow_base < 0 ? -1 : oc.prow_base + (i * G + jh) * Hkv;
+                        em.rows.push_back(r);
+                    }
                 cur_rows += ni * G;
             }
         }
-        if (cur_n) {
-            groups.push_back({cur_off, cur_n});
-            group_rows.push_back(cur_rows);
-        }
+        if (cur_rows) groups.push_back({cur_off, cur_rows});
         for (int32_t h = 0; h < Hkv; ++h) {
             for (size_t gi = 0; gi < groups.size(); ++gi) {
                 fa::Item it;
                 std::memset(&it, 0, sizeof it);
                 it.chunk = int32_t(c);
                 it.head = h;
-                it.ent_off = groups[gi].first;
-                it.n_ent = groups[gi].second;
-                it.n_rows = group_rows[gi];
+                it.row_off = groups[gi].first;
+                it.n_rows = groups[gi].second;
                 const int64_t kv = int64_t(ch.n_pages) * kPageSize * fa::kHeadDim * 2 * 2;
                 if (tc) {
                     em.items_tc.push_back(it);
@@ -386,6 +382,7 @@ int build_plan(Input &in, const fa_plan_opts &opts, fa_plan *plan) {
                 }
             }
         }
+        if (em.rows.size() > size_t(INT32_MAX)) return FA_ERR_UNSUPPORTED;
     }
 
     st.num_chunks = int64_t(em.chunks.size());
@@ -404,10 +401,9 @@ int build_plan(Input &in, const fa_plan_opts &opts, fa_plan *plan) {
     auto place = [&](int64_t bytes) { const int64_t at = off; off = align_up(off + std::max<int64_t>(bytes, 1)); return at; };
     L.chunk_pages = place(int64_t(em.chunk_pages.size()) * 4);
     L.chunks = place(int64_t(em.chunks.size()) * sizeof(fa::Chunk));
-    L.occs = place(int64_t(em.occs.size()) * sizeof(fa::Occ));
     L.items_rows = place(int64_t(em.items_rows.size()) * sizeof(fa::Item));
     L.items_tc = place(int64_t(em.items_tc.size()) * sizeof(fa::Item));
-    L.ents = place(int64_t(em.ents.size()) * sizeof(fa::Ent));
+    L.rows = place(int64_t(em.rows.size()) * sizeof(fa::RowRec));
     L.branches = place(int64_t(em.branches.size()) * sizeof(fa::Branch));
     L.q_branch = place(int64_t(em.q_branch.size()) * 4);
     L.merge_bases = place(int64_t(em.merge_bases.size()) * 4);
@@ -415,10 +411,9 @@ int build_plan(Input &in, const fa_plan_opts &opts, fa_plan *plan) {
     L.total = off;
     L.n_chunk_pages = int32_t(em.chunk_pages.size());
     L.n_chunks = int32_t(em.chunks.size());
-    L.n_occs = int32_t(em.occs.size());
     L.n_items_rows = int32_t(em.items_rows.size());
     L.n_items_tc = int32_t(em.items_tc.size());
-    L.n_ents = int32_t(em.ents.size());
+    L.n_rows = int32_t(em.rows.size());
     L.n_branches = B;
     L.total_q = in.q_off[B];
     L.n_merge_bases = int32_t(em.merge_bases.size());
@@ -427,10 +422,9 @@ int build_plan(Input &in, const fa_plan_opts &opts, fa_plan *plan) {
     auto put = [&](int64_t at, const void *src, size_t bytes) { if (bytes) std::memcpy(plan->blob.data() + at, src, bytes); };
     put(L.chunk_pages, em.chunk_pages.data(), em.chunk_pages.size() * 4);
     put(L.chunks, em.chunks.data(), em.chunks.size() * sizeof(fa::Chunk));
-    put(L.occs, em.occs.data(), em.occs.size() * sizeof(fa::Occ));
     put(L.items_rows, em.items_rows.data(), em.items_rows.size() * sizeof(fa::Item));
     put(L.items_tc, em.items_tc.data(), em.items_tc.size() * sizeof(fa::Item));
-    put(L.ents, em.ents.data(), em.ents.size() * sizeof(fa::Ent));
+    put(L.rows, em.rows.data(), em.rows.size() * sizeof(fa::RowRec));
     put(L.branches, em.branches.data(), em.branches.size() * sizeof(fa::Branch));
     put(L.q_branch, em.q_branch.data(), em.q_branch.size() * 4);
     put(L.merge_bases, em.merge_bases.data(), em.merge_bases.size() * 4);

@@ -10,6 +10,7 @@ constexpr int kPageSize = 16;
 constexpr int kRowsMax = 32;      // rows of one row-kernel work item (two m16 tiles)
 constexpr int kTcRows = 128;      // rows of one tcgen05 work item (one M = 128 tile)
 constexpr int kAlign = 256;       // byte alignment of every array in the plan blob
+constexpr int kMaxChunkPages = 256;  // longest chunk the planner cuts (the tcgen05 kernel's limit)
 
 // A chunk: consecutive physical pages chunk_pages[page_off .. page_off + n_pages) that every
 // one of its readers sees as consecutive logical positions.  Its readers ("occurrences")
@@ -21,11 +22,12 @@ struct Chunk {
     int32_t n_occ;
 };
 
-// One reader of one chunk: branch `branch` sees slot s of the chunk's page k at logical
-// position lpos0 + 16 k + s.  mask_off: word offset of its visibility words (bit 16 k + s),
-// or -1 when every slot of the chunk is valid and visible to it.  prow_base: first fp32
-// partial row of this occurrence for KV head 0 (rows of head g start at prow_base +
-// g * n_q * G), or -1 when the occurrence is the branch's only one and writes `out` directly.
+// One reader of one chunk (host side only): branch `branch` sees slot s of the chunk's page
+// k at logical position lpos0 + 16 k + s.  mask_off: word offset of its visibility words
+// (bit 16 k + s), or -1 when every slot of the chunk is valid and visible to it.
+// prow_base: its first fp32 partial row, or -1 when the occurrence is the branch's only one
+// and writes `out` directly.  Partial row of (query token i, head-in-group jh, KV head g):
+// prow_base + (i * G + jh) * Hkv + g.
 struct Occ {
     int32_t branch;
     int32_t lpos0;
@@ -33,23 +35,24 @@ struct Occ {
     int32_t prow_base;
 };
 
-// A work item: one chunk, one KV head, and a row group = entries ents[ent_off ..
-// ent_off + n_ent), together n_rows = sum(ni) * G rows.
+// A work item: one chunk, one KV head, and a row group = rows[row_off .. row_off + n_rows)
+// (row groups are shared by every KV head of a chunk).
 struct Item {
     int32_t chunk;
     int32_t head;
-    int32_t ent_off;
-    int32_t n_ent;
+    int32_t row_off;
     int32_t n_rows;
-    int32_t pad[3];
 };
 
-// Query tokens i0 .. i0 + ni - 1 of occurrence `occ`.
-struct Ent {
-    int32_t occ;
-    int32_t i0;
-    int32_t ni;
-    int32_t pad;
+// One stacked query row of a row group: a (reader, query token, query head in the GQA group).
+// For KV head g: its q / out / lse row is qrow0 + g * G, its partial row prow0 + g (prow0 = -1:
+// a direct write).  climit: chunk tokens t <= climit are causally visible.  mask_off: the
+// reader's visibility words for the chunk, -1 = all visible.
+struct RowRec {
+    int32_t qrow0;
+    int32_t climit;
+    int32_t mask_off;
+    int32_t prow0;
 };
 
 // Per branch: its query rows start at q_begin (token index into q/out), n_q of them, the
@@ -69,10 +72,10 @@ struct Branch {
 // Byte offsets of the arrays inside the device plan buffer.  The first 256 bytes hold the
 // device error word (int32 at offset 0).
 struct Layout {
-    int64_t chunk_pages, chunks, occs, items_rows, items_tc, ents, branches, q_branch,
-        merge_bases, mask_words, total;
-    int32_t n_chunk_pages, n_chunks, n_occs, n_items_rows, n_items_tc, n_ents, n_branches,
-        total_q, n_merge_bases, n_mask_words;
+    int64_t chunk_pages, chunks, items_rows, items_tc, rows, branches, q_branch, merge_bases,
+        mask_words, total;
+    int32_t n_chunk_pages, n_chunks, n_items_rows, n_items_tc, n_rows, n_branches, total_q,
+        n_merge_bases, n_mask_words;
 };
 
 // Device error word bits.

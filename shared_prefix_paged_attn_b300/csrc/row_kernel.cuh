@@ -79,15 +79,23 @@ __device__ __forceinline__ void run_pages(const DecodeParams &p, Smem &sm, const
     const uint32_t ring = ptx::smem_u32(sm.ring) + warp * kStages * kSlotBytes;
     const uint32_t qs = ptx::smem_u32(sm.qs);
 
+    // page ids of this warp's pages (k = warp + 4 i): lane l holds index i = 32 b + l of the
+    // current batch b, and the next batch is already loaded, so issuing never waits on them
+    auto pid_at = [&](int i) -> int32_t {
+        const int k = warp + kWarps * i;
+        return k < n_pages ? __ldg(pages + k) : 0;
+    };
+    int32_t pid_cur = pid_at(lane), pid_nxt = pid_at(32 + lane);
     int issued = 0;
-    if (lane == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            const int k = warp + kWarps * s;
-            if (k < n_pages)
-                issue_page(p, ring + s * kSlotBytes, ptx::smem_u32(&sm.bars[warp][s]), it.head, pages[k]);
+#pragma unroll
+    for (int s = 0; s < kStages; ++s) {
+        const int k = warp + kWarps * s;
+        const int32_t page = __shfl_sync(0xffffffffu, pid_cur, s);
+        if (k < n_pages) {
+            if (lane == 0) issue_page(p, ring + s * kSlotBytes, ptx::smem_u32(&sm.bars[warp][s]), it.head, page);
+            ++issued;
         }
     }
-    for (int s = 0; s < kStages; ++s) issued += (warp + kWarps * s < n_pages);
 
     int32_t moff[2][2], clim[2][2];
 #pragma unroll
@@ -210,9 +218,15 @@ __device__ __forceinline__ void run_pages(const DecodeParams &p, Smem &sm, const
         }
 
         __syncwarp();
+        const int in_ = j + kStages;  // index of the next page in this warp's list
+        if ((in_ & 31) == 0) {
+            pid_cur = pid_nxt;
+            pid_nxt = pid_at(in_ + 32 + lane);
+        }
+        const int32_t page = __shfl_sync(0xffffffffu, pid_cur, in_ & 31);
         const int kn = k + kWarps * kStages;
         if (kn < n_pages) {
-            if (lane == 0) issue_page(p, kb, bar, it.head, pages[kn]);
+            if (lane == 0) issue_page(p, kb, bar, it.head, page);
             ++issued;
         }
     }
@@ -237,25 +251,16 @@ __global__ void __launch_bounds__(kThreads, 2) row_kernel(const __grid_constant_
             for (int s = 0; s < kStages; ++s) ptx::mbar_init(ptx::smem_u32(&sm.bars[w][s]), 1);
         ptx::fence_mbar_init();
     }
-    // row table: row r of the item -> (reader, query token i, head-in-group j)
+    // the item's row records: one 16-byte load per row
     bool row_needs_mask = false;
     if (tid < kRowsMax) {
         RowInfo ri{0, 0x3fffffff, -1, -1};
         if (tid < it.n_rows) {
-            int e = it.ent_off, acc = 0;
-            Ent en = p.ents[e];
-            while (tid >= acc + en.ni * p.G) {
-                acc += en.ni * p.G;
-                en = p.ents[++e];
-            }
-            const int i = en.i0 + (tid - acc) / p.G;
-            const int jh = (tid - acc) % p.G;
-            const Occ oc = p.occs[en.occ];
-            const Branch br = p.branches[oc.branch];
-            ri.qrow = (br.q_begin + i) * p.Hq + it.head * p.G + jh;
-            ri.climit = br.qpos0 + i - oc.lpos0;
-            ri.mask_off = oc.mask_off;
-            ri.prow = oc.prow_base < 0 ? -1 : oc.prow_base + it.head * (br.n_q * p.G) + i * p.G + jh;
+            const int4 rec = __ldg(reinterpret_cast<const int4 *>(p.rows + it.row_off + tid));
+            ri.qrow = rec.x + it.head * p.G;
+            ri.climit = rec.y;
+            ri.mask_off = rec.z;
+            ri.prow = rec.w < 0 ? -1 : rec.w + it.head;
             row_needs_mask = ri.mask_off >= 0 || ri.climit < kPageSize * ch.n_pages - 1;
         }
         sm.rows[tid] = ri;

@@ -9,11 +9,13 @@
 // of Q, so S = Q K^T and O += P V are dense M = 128 contractions on tcgen05.
 //
 // One CTA = 12 warps per work item (chunk x KV head x row group of <= 256 rows):
-//   warp 0 (one thread)  TMA producer: per 128-token tile, the 8 pages of K (and of V) as
-//                        2 KiB boxes (64 dims x 16 tokens, 128-byte swizzle) into a 3-stage
-//                        K ring and a 2-stage V ring; pages past the chunk's end are read at
-//                        an out-of-range page index, which the copy fills with zeros;
-//   warp 1 (one thread)  MMA issuer; the whole warp allocates the 512 TMEM columns:
+//   warps 0 and 2        TMA producers: per 128-token tile, warp 0 loads the 8 pages of K as
+//                        2 KiB boxes (64 dims x 16 tokens, 128-byte swizzle) into a 2-stage
+//                        K ring, warp 2 the 8 pages of V as whole 4 KiB page boxes into a
+//                        3-stage V ring; pages past the chunk's end are read at an
+//                        out-of-range page index, which the copy fills with zeros;
+//   warp 1               MMA issuer (one lane issues, the warp waits converged); the
+//                        whole warp allocates the 512 TMEM columns:
 //                        O0 [0,128) O1 [128,256) S0/P0 [256,384) S1/P1 [384,512);
 //   warps 4-7, 8-11      softmax of M tile 0 and 1 (one row per thread, TMEM lane = row):
 //                        S from TMEM, mask (visibility words, chunk end, causal limit), base-2
@@ -36,11 +38,19 @@ constexpr int kTilePages = 8;
 constexpr int kTileTok = kTilePages * kPageSize;   // 128 tokens per KV tile
 constexpr int kHalfBytes = kTileTok * 128;          // 64 dims of 128 tokens: 16 KiB
 constexpr int kTileBytes = 2 * kHalfBytes;          // 32 KiB per tile of K (or V)
-constexpr int kKStages = 3;
-constexpr int kVStages = 2;
+constexpr int kKStages = 2;
+constexpr int kVStages = 3;
 constexpr int kRows = 2 * kTcRows;                  // 256 rows per work item
 constexpr int kQHalf = kRows * 128;                 // 64 dims of 256 rows: 32 KiB
 constexpr int kThreads = 384;
+// Register split (setmaxnreg): the block launches with kLaunchRegs per thread; warpgroup 0
+// (producer, MMA, two idle warps) gives registers back, the two softmax warpgroups take
+// more.  128 * kLowRegs + 256 * kHighRegs must not exceed 384 * (launch registers), which
+// the host checks against the compiled kernel before the first launch.
+constexpr int kLaunchRegs = 168;
+constexpr int kLowRegs = 56;
+constexpr int kHighRegs = 208;
+static_assert(128 * kLowRegs + 256 * kHighRegs <= kThreads * kLaunchRegs, "register split fits the launch");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0, kColS = 256;
 
@@ -81,134 +91,157 @@ struct Row {
 
 // Row r of a work item -> (query row, causal limit in chunk tokens, visibility words, partial row).
 __device__ __forceinline__ Row item_row(const DecodeParams &p, const Item &it, int r) {
-    int e = it.ent_off, acc = 0;
-    Ent en = p.ents[e];
-    while (r >= acc + en.ni * p.G) {
-        acc += en.ni * p.G;
-        en = p.ents[++e];
-    }
-    const int i = en.i0 + (r - acc) / p.G;
-    const int jh = (r - acc) % p.G;
-    const Occ oc = p.occs[en.occ];
-    const Branch br = p.branches[oc.branch];
-    Row x;
-    x.qrow = (br.q_begin + i) * p.Hq + it.head * p.G + jh;
-    x.climit = br.qpos0 + i - oc.lpos0;
-    x.mask_off = oc.mask_off;
-    x.prow = oc.prow_base < 0 ? -1 : oc.prow_base + it.head * (br.n_q * p.G) + i * p.G + jh;
-    return x;
+    const int4 rec = __ldg(reinterpret_cast<const int4 *>(p.rows + it.row_off + r));
+    return Row{rec.x + it.head * p.G, rec.y, rec.z, rec.w < 0 ? -1 : rec.w + it.head};
 }
 
-__device__ __forceinline__ void load_tile(const DecodeParams &p, const CUtensorMap *map, uint32_t dst,
-                                          uint32_t bar, const int32_t *pages, int n_pages, int j, int head) {
-    ptx::mbar_arrive_expect_tx(bar, kTileBytes);
-#pragma unroll 1
-    for (int pg = 0; pg < kTilePages; ++pg) {
-        const int idx = j * kTilePages + pg;
-        const int page = idx < n_pages ? pages[idx] : p.pool_pages;  // out of range: zero fill
-        ptx::tma_load_4d(dst + pg * 2048, map, bar, 0, 0, head, page);
-        ptx::tma_load_4d(dst + kHalfBytes + pg * 2048, map, bar, 64, 0, head, page);
+// Producer warp: lanes 0-7 each read one page id of the tile and issue that page's two
+// boxes (64 dims each); lane 0 arms the mbarrier first.  Pages past the chunk end are read
+// at an out-of-range page index, which the copy fills with zeros.
+// K tile: [half][128 tokens][64 dims] (two boxes per page), so that a QK^T MMA with N = 128
+// tokens sees 8-token groups at a uniform 1 KiB stride.
+__device__ __forceinline__ void load_k_tile(const CUtensorMap *map, uint32_t dst, uint32_t bar, int32_t page,
+                                            int head, int lane) {
+    if (lane == 0) ptx::mbar_arrive_expect_tx(bar, kTileBytes);
+    __syncwarp();
+    if (lane < kTilePages) {
+        ptx::tma_load_4d(dst + lane * 2048, map, bar, 0, 0, head, page);
+        ptx::tma_load_4d(dst + kHalfBytes + lane * 2048, map, bar, 64, 0, head, page);
     }
+    __syncwarp();
 }
 
-__device__ void producer(const DecodeParams &p, Smem &sm, const Item &it, const Chunk &ch, int T) {
+// V tile: [page][half][16 tokens][64 dims] (one box per page); a P V MMA step covers one page.
+__device__ __forceinline__ void load_v_tile(const CUtensorMap *map, uint32_t dst, uint32_t bar, int32_t page,
+                                            int head, int lane) {
+    if (lane == 0) ptx::mbar_arrive_expect_tx(bar, kTileBytes);
+    __syncwarp();
+    if (lane < kTilePages) ptx::tma_load_5d(dst + lane * 4096, map, bar, 0, 0, 0, head, page);
+    __syncwarp();
+}
+
+// Producer warps: warp 0 streams K tiles into a 2-stage ring, warp 2 streams V tiles into a
+// 3-stage ring (V stays alive one pipeline step longer than K), each running ahead as far as
+// its ring allows.
+template <bool kIsV>
+__device__ __forceinline__ void producer(const DecodeParams &p, Smem &sm, const Item &it, const Chunk &ch, int T,
+                                         int lane) {
+    constexpr int NS = kIsV ? kVStages : kKStages;
     const int32_t *pages = p.chunk_pages + ch.page_off;
     const volatile int32_t *abort = &sm.abort;
-    int k_issued = 0, v_issued = 0;
-    // K runs one tile ahead of V: K0, K1, V0, K2, V1, ...
-    load_tile(p, &p.kmap, ptx::smem_u32(sm.k[0]), ptx::smem_u32(&sm.kfull[0]), pages, ch.n_pages, 0, it.head);
-    k_issued = 1;
-    for (int j = 0; j < T; ++j) {
-        const int jk = j + 1;
-        if (jk < T) {
-            const int s = jk % kKStages;
-            if (jk >= kKStages && !wait_bar(ptx::smem_u32(&sm.kfree[s]), (jk / kKStages - 1) & 1, abort)) break;
-            load_tile(p, &p.kmap, ptx::smem_u32(sm.k[s]), ptx::smem_u32(&sm.kfull[s]), pages, ch.n_pages, jk,
-                      it.head);
-            ++k_issued;
-        }
-        const int s = j % kVStages;
-        if (j >= kVStages && !wait_bar(ptx::smem_u32(&sm.vfree[s]), (j / kVStages - 1) & 1, abort)) break;
-        load_tile(p, &p.vmap, ptx::smem_u32(sm.v[s]), ptx::smem_u32(&sm.vfull[s]), pages, ch.n_pages, j, it.head);
-        ++v_issued;
+    const CUtensorMap *map = kIsV ? &p.vmap_page : &p.kmap;
+    if (lane == 0) ptx::prefetch_tmap(map);
+    // every page id of the chunk (<= 256 = 8 x 32) up front: lane l holds pages l + 32 i
+    int32_t pid[kMaxChunkPages / 32];
+#pragma unroll
+    for (int i = 0; i < kMaxChunkPages / 32; ++i) {
+        const int idx = 32 * i + lane;
+        pid[i] = idx < ch.n_pages ? __ldg(pages + idx) : p.pool_pages;
     }
-    if (k_issued < T || v_issued < T) fail(sm, p.err);
-    // every copy this CTA started must land before its shared memory goes away
+    // page of tile j seen by lane l < 8: index 8 j + l, held by lane 8 (j % 4) + l in pid[j / 4]
+    auto page_of = [&](int j) -> int32_t {
+        const int q = j >> 2;
+        int32_t v = pid[0];
+#pragma unroll
+        for (int i = 1; i < kMaxChunkPages / 32; ++i)
+            if (q == i) v = pid[i];
+        v = __shfl_sync(0xffffffffu, v, 8 * (j & 3) + (lane & 7));
+        return (j * kTilePages + lane < ch.n_pages) ? v : p.pool_pages;
+    };
+    int issued = 0;
+    bool ok = true;
+    for (int j = 0; j < T; ++j) {
+        const int32_t page = page_of(j);
+        const int s = j % NS;
+        uint64_t &free_bar = kIsV ? sm.vfree[s] : sm.kfree[s];
+        uint64_t &full_bar = kIsV ? sm.vfull[s] : sm.kfull[s];
+        if (j >= NS) ok = __all_sync(0xffffffffu, wait_bar(ptx::smem_u32(&free_bar), (j / NS - 1) & 1, abort));
+        if (!ok) break;
+        if (kIsV)
+            load_v_tile(map, ptx::smem_u32(sm.v[s]), ptx::smem_u32(&full_bar), page, it.head, lane);
+        else
+            load_k_tile(map, ptx::smem_u32(sm.k[s]), ptx::smem_u32(&full_bar), page, it.head, lane);
+        ++issued;
+    }
+    if (issued < T && lane == 0) fail(sm, p.err);
+    // every copy this warp started must land before the CTA's shared memory goes away
     const volatile int32_t never = 0;
-    for (int j = (k_issued > kKStages ? k_issued - kKStages : 0); j < k_issued; ++j)
-        wait_bar(ptx::smem_u32(&sm.kfull[j % kKStages]), (j / kKStages) & 1, &never);
-    for (int j = (v_issued > kVStages ? v_issued - kVStages : 0); j < v_issued; ++j)
-        wait_bar(ptx::smem_u32(&sm.vfull[j % kVStages]), (j / kVStages) & 1, &never);
+    for (int j = (issued > NS ? issued - NS : 0); j < issued; ++j)
+        wait_bar(ptx::smem_u32(kIsV ? &sm.vfull[j % NS] : &sm.kfull[j % NS]), (j / NS) & 1, &never);
 }
 
-__device__ void mma_issuer(Smem &sm, uint32_t tmem, int T, int MT) {
+// MMA warp: every lane waits on the barriers (the warp stays converged); lane 0 issues the
+// MMAs and the commits.
+__device__ __forceinline__ void mma_issuer(Smem &sm, uint32_t tmem, int T, int MT, int lane) {
     const volatile int32_t *abort = &sm.abort;
     const uint32_t qa = ptx::smem_u32(sm.q);
     bool ok = true;
-    auto pv = [&](int m, int j) {  // O_m (+)= P_m V_j
-        const uint32_t vb = ptx::smem_u32(sm.v[j % kVStages]);
-#pragma unroll
-        for (int kk = 0; kk < kTilePages; ++kk)
-            tc::mma_ts(tmem + kColO + 128 * m, tmem + kColS + 128 * m + 8 * kk,
-                       tc::sdesc_sw128(vb + kk * 2048, kHalfBytes, 1024), kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
-        tc::commit(ptx::smem_u32(&sm.odone[m]));
+    auto wait = [&](uint64_t &bar, uint32_t parity) {
+        ok = __all_sync(0xffffffffu, wait_bar(ptx::smem_u32(&bar), parity, abort));
+        return ok;
     };
-    for (int j = 0; j < T && ok; ++j) {
-        for (int m = 0; m < MT && ok; ++m) {
-            if (j > 0) {
-                if (m == 0 && !wait_bar(ptx::smem_u32(&sm.vfull[(j - 1) % kVStages]), ((j - 1) / kVStages) & 1, abort)) {
-                    ok = false;
-                    break;
-                }
-                if (!wait_bar(ptx::smem_u32(&sm.pfull[m]), (j - 1) & 1, abort)) {
-                    ok = false;
-                    break;
-                }
-                tc::fence_after();
-                pv(m, j - 1);
-            }
-            if (m == 0) {
-                if (!wait_bar(ptx::smem_u32(&sm.kfull[j % kKStages]), (j / kKStages) & 1, abort)) {
-                    ok = false;
-                    break;
-                }
-                tc::fence_after();
-            }
+    auto pv = [&](int m, int j) {  // O_m (+)= P_m V_j
+        if (lane == 0) {
+            const uint32_t vb = ptx::smem_u32(sm.v[j % kVStages]);
+#pragma unroll
+            for (int kk = 0; kk < kTilePages; ++kk)
+                tc::mma_ts(tmem + kColO + 128 * m, tmem + kColS + 128 * m + 8 * kk,
+                           tc::sdesc_sw128(vb + kk * 4096, 2048, 1024), kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+            tc::commit(ptx::smem_u32(&sm.odone[m]));
+        }
+        __syncwarp();
+    };
+    auto qk = [&](int m, int j) {  // S_m = Q_m K_j^T
+        if (lane == 0) {
             const uint32_t kb = ptx::smem_u32(sm.k[j % kKStages]);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
                 const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-                tc::mma_ss(tmem + kColS + 128 * m, tc::sdesc_sw128(qa + (kk >> 2) * kQHalf + m * (kQHalf / 2) + (kk & 3) * 32, 16, 1024),
+                tc::mma_ss(tmem + kColS + 128 * m,
+                           tc::sdesc_sw128(qa + (kk >> 2) * kQHalf + m * (kQHalf / 2) + (kk & 3) * 32, 16, 1024),
                            tc::sdesc_sw128(kb + off, 16, 1024), kIdescQK, kk > 0 ? 1u : 0u);
             }
             tc::commit(ptx::smem_u32(&sm.sfull[m]));
         }
-        if (!ok) break;
-        tc::commit(ptx::smem_u32(&sm.kfree[j % kKStages]));
-        if (j > 0) tc::commit(ptx::smem_u32(&sm.vfree[(j - 1) % kVStages]));
-    }
-    if (ok) {
-        if (wait_bar(ptx::smem_u32(&sm.vfull[(T - 1) % kVStages]), ((T - 1) / kVStages) & 1, abort)) {
-            for (int m = 0; m < MT && ok; ++m) {
-                if (!wait_bar(ptx::smem_u32(&sm.pfull[m]), (T - 1) & 1, abort)) {
-                    ok = false;
-                    break;
-                }
+        __syncwarp();
+    };
+    for (int j = 0; j < T && ok; ++j) {
+        for (int m = 0; m < MT && ok; ++m) {
+            if (j > 0) {
+                if (m == 0 && !wait(sm.vfull[(j - 1) % kVStages], ((j - 1) / kVStages) & 1)) break;
+                if (!wait(sm.pfull[m], (j - 1) & 1)) break;
                 tc::fence_after();
-                pv(m, T - 1);
+                pv(m, j - 1);
             }
-        } else {
-            ok = false;
+            if (m == 0) {
+                if (!wait(sm.kfull[j % kKStages], (j / kKStages) & 1)) break;
+                tc::fence_after();
+            }
+            qk(m, j);
+        }
+        if (!ok) break;
+        if (lane == 0) {
+            tc::commit(ptx::smem_u32(&sm.kfree[j % kKStages]));
+            if (j > 0) tc::commit(ptx::smem_u32(&sm.vfree[(j - 1) % kVStages]));
+        }
+        __syncwarp();
+    }
+    if (ok && wait(sm.vfull[(T - 1) % kVStages], ((T - 1) / kVStages) & 1)) {
+        for (int m = 0; m < MT; ++m) {
+            if (!wait(sm.pfull[m], (T - 1) & 1)) break;
+            tc::fence_after();
+            pv(m, T - 1);
         }
     }
-    if (!ok) *reinterpret_cast<volatile int32_t *>(&sm.abort) = 1;
-    // all MMAs issued by this thread are complete before TMEM is freed
-    tc::commit(ptx::smem_u32(&sm.fin));
+    if (!ok && lane == 0) *reinterpret_cast<volatile int32_t *>(&sm.abort) = 1;
+    // all MMAs issued by this warp are complete before TMEM is freed
+    if (lane == 0) tc::commit(ptx::smem_u32(&sm.fin));
+    __syncwarp();
     const volatile int32_t never = 0;
     wait_bar(ptx::smem_u32(&sm.fin), 0, &never);
 }
 
-__device__ void softmax(const DecodeParams &p, Smem &sm, const Chunk &ch, const Row &ri, bool valid, uint32_t tmem,
+__device__ __forceinline__ void softmax(const DecodeParams &p, Smem &sm, const Chunk &ch, const Row &ri, bool valid, uint32_t tmem,
                         int T, int m, int wq, int lane) {
     const volatile int32_t *abort = &sm.abort;
     const uint32_t lane_base = uint32_t(wq * 32) << 16;
@@ -220,17 +253,21 @@ __device__ void softmax(const DecodeParams &p, Smem &sm, const Chunk &ch, const 
     float mrun = -INFINITY, lrun = 0.f;
     bool ok = true;
 
+    if (!__any_sync(0xffffffffu, valid)) {
+        // a warp of padding rows only keeps the barrier protocol: its rows are never written
+        for (int j = 0; j < T && ok; ++j) {
+            ok = __all_sync(0xffffffffu, wait_bar(ptx::smem_u32(&sm.sfull[m]), j & 1, abort));
+            if (ok) ptx::mbar_arrive(ptx::smem_u32(&sm.pfull[m]));
+        }
+        if (!ok && lane == 0) fail(sm, p.err);
+        return;
+    }
     for (int j = 0; j < T; ++j) {
-        ok = __all_sync(0xffffffffu, wait_bar(ptx::smem_u32(&sm.sfull[m]), j & 1, abort));
-        if (!ok) break;
-        tc::fence_after();
-
         // visibility of the tile's 128 tokens for this row: words of the reader, chunk end,
-        // causal limit (all ones when nothing is masked)
+        // causal limit; computed while the MMA runs
         const int t0 = j * kTileTok;
         uint32_t bits[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
-        const bool masked = valid && (ri.mask_off >= 0 || t0 + kTileTok > n_tok || ri.climit < t0 + kTileTok - 1);
-        if (masked) {
+        if (valid && (ri.mask_off >= 0 || t0 + kTileTok > n_tok || ri.climit < t0 + kTileTok - 1)) {
 #pragma unroll
             for (int w = 0; w < 4; ++w) {
                 const int tq = t0 + 32 * w;
@@ -246,42 +283,68 @@ __device__ void softmax(const DecodeParams &p, Smem &sm, const Chunk &ch, const 
                 bits[w] = b;
             }
         }
-        const bool any_masked = __any_sync(0xffffffffu, masked);
+        ok = __all_sync(0xffffffffu, wait_bar(ptx::smem_u32(&sm.sfull[m]), j & 1, abort));
+        if (!ok) break;
+        tc::fence_after();
+        uint32_t s[128];
+        tc::ld32(tS + 0, s + 0);
+        tc::ld32(tS + 32, s + 32);
+        tc::ld32(tS + 64, s + 64);
+        tc::ld32(tS + 96, s + 96);
+        tc::ld_wait();
+        tc::tie32(s + 0);
+        tc::tie32(s + 32);
+        tc::tie32(s + 64);
+        tc::tie32(s + 96);
 
-        // pass 1: row max over the visible scores (32 columns at a time, next load in flight)
-        float mx = -INFINITY;
-        {
-            uint32_t a[32], b[32];
-            tc::ld32(tS, a);
-            tc::ld_wait();
-            tc::tie32(a);
+        if (__any_sync(0xffffffffu, (bits[0] & bits[1] & bits[2] & bits[3]) != 0xffffffffu)) {
 #pragma unroll
-            for (int h = 0; h < 4; ++h) {
-                if (h < 3) tc::ld32(tS + 32 * (h + 1), b);
-                if (any_masked) {
-#pragma unroll
-                    for (int c = 0; c < 32; ++c)
-                        if (!((bits[h] >> c) & 1u)) a[c] = __float_as_uint(-INFINITY);
-                }
-#pragma unroll
-                for (int c = 0; c < 32; ++c) mx = fmaxf(mx, __uint_as_float(a[c]));
-                if (h < 3) {
-                    tc::ld_wait();
-                    tc::tie32(b);
-#pragma unroll
-                    for (int c = 0; c < 32; ++c) a[c] = b[c];
-                }
-            }
+            for (int c = 0; c < 128; ++c)
+                if (!((bits[c >> 5] >> (c & 31)) & 1u)) s[c] = __float_as_uint(-INFINITY);
         }
-        if (!valid) mx = -INFINITY;
+        // row max with eight independent chains (short dependency latency)
+        float mxk[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mxk[k] = __uint_as_float(s[k]);
+#pragma unroll
+        for (int c = 8; c < 128; c += 8)
+#pragma unroll
+            for (int k = 0; k < 8; ++k) mxk[k] = fmaxf(mxk[k], __uint_as_float(s[c + k]));
+        float mx = fmaxf(fmaxf(fmaxf(mxk[0], mxk[1]), fmaxf(mxk[2], mxk[3])),
+                         fmaxf(fmaxf(mxk[4], mxk[5]), fmaxf(mxk[6], mxk[7])));
+        if (!valid) mx = 0.f;  // a padding row (zero Q) in a warp with real rows: finite junk
         const float mnew = fmaxf(mrun, mx * sl2);
-        const bool want = mrun != -INFINITY && mnew > mrun + 8.0f;
-        if (__any_sync(0xffffffffu, want)) {
-            // raise the running max of this warp's rows; O of the previous tiles is rescaled
-            float alpha = 1.f;
+        // lazy rescale: the running max is only raised when it grows by more than 2^8
+        const bool rescale = __any_sync(0xffffffffu, mrun != -INFINITY && mnew > mrun + 8.0f);
+        float alpha = 1.f;
+        if (rescale) {
             if (mrun != -INFINITY && mnew > mrun) alpha = ptx::ex2(mrun - mnew);
             if (mnew > mrun) mrun = mnew;
             lrun *= alpha;
+        } else if (mrun == -INFINITY) {
+            mrun = mnew;
+        }
+        const float muse = mrun == -INFINITY ? 0.f : mrun;
+
+        // P = 2^(s * scale * log2 e - m) as bf16 pairs over the first 64 columns of S
+        float rsk[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+                const float x = ptx::ex2(fmaf(__uint_as_float(s[32 * h + 2 * c]), sl2, -muse));
+                const float y = ptx::ex2(fmaf(__uint_as_float(s[32 * h + 2 * c + 1]), sl2, -muse));
+                rsk[c & 7] += x + y;
+                pk[c] = ptx::pack_bf16(x, y);
+            }
+            // columns 16h .. 16h+15 held scores already in registers
+            tc::st16(tS + 16 * h, pk);
+        }
+        lrun += ((rsk[0] + rsk[1]) + (rsk[2] + rsk[3])) + ((rsk[4] + rsk[5]) + (rsk[6] + rsk[7]));
+
+        if (rescale) {
+            // O of the previous tiles (the P V MMA of tile j-1 must be done) times alpha
             ok = __all_sync(0xffffffffu, wait_bar(ptx::smem_u32(&sm.odone[m]), (j - 1) & 1, abort));
             if (!ok) break;
             tc::fence_after();
@@ -295,48 +358,7 @@ __device__ void softmax(const DecodeParams &p, Smem &sm, const Chunk &ch, const 
                 for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
                 tc::st32(tO + 32 * h, o);
             }
-        } else if (mrun == -INFINITY) {
-            mrun = mnew;
         }
-        const float muse = mrun == -INFINITY ? 0.f : mrun;
-
-        // pass 2: P = 2^(s * scale * log2 e - m) as bf16 pairs over S's first 64 columns
-        float rs = 0.f;
-        {
-            uint32_t a[32], b[32];
-            tc::ld32(tS, a);
-            tc::ld_wait();
-            tc::tie32(a);
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
-                if (h < 3) tc::ld32(tS + 32 * (h + 1), b);
-                if (any_masked) {
-#pragma unroll
-                    for (int c = 0; c < 32; ++c)
-                        if (!((bits[h] >> c) & 1u)) a[c] = __float_as_uint(-INFINITY);
-                }
-                uint32_t pk[16];
-#pragma unroll
-                for (int c = 0; c < 16; ++c) {
-                    float x = 0.f, y = 0.f;
-                    if (valid) {
-                        x = ptx::ex2(fmaf(__uint_as_float(a[2 * c]), sl2, -muse));
-                        y = ptx::ex2(fmaf(__uint_as_float(a[2 * c + 1]), sl2, -muse));
-                    }
-                    rs += x + y;
-                    pk[c] = ptx::pack_bf16(x, y);
-                }
-                // columns 16h .. 16h+15 held scores 16h .. 16h+15, already read
-                tc::st16(tS + 16 * h, pk);
-                if (h < 3) {
-                    tc::ld_wait();
-                    tc::tie32(b);
-#pragma unroll
-                    for (int c = 0; c < 32; ++c) a[c] = b[c];
-                }
-            }
-        }
-        lrun += rs;
         tc::st_wait();
         tc::fence_before();
         ptx::mbar_arrive(ptx::smem_u32(&sm.pfull[m]));
@@ -401,6 +423,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
     const Chunk ch = p.chunks[it.chunk];
     const int T = (ch.n_pages + kTilePages - 1) / kTilePages;
     const int MT = it.n_rows > kTcRows ? 2 : 1;
+    if (ch.n_pages > kMaxChunkPages || it.n_rows > kRows) {  // never planned; refuse, uniformly
+        if (threadIdx.x == 0) atomicOr(p.err, kErrBounds);
+        return;
+    }
 
     if (tid == 0) {
         for (int s = 0; s < kKStages; ++s) {
@@ -428,8 +454,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
     // 128-byte swizzled K-major (zeros for padding rows)
     Row ri{0, 0x3fffffff, -1, -1};
     bool valid = false;
+    const int sm_m = (warp >> 2) - 1;  // softmax warpgroup = M tile (warps 4-7, 8-11)
     if (warp >= 4) {
-        const int r = tid - 128;
+        // TMEM lane quarter of a warp is warp % 4, so row = 128 m + 32 (warp % 4) + lane
+        const int r = sm_m * kTcRows + (warp & 3) * 32 + lane;
         valid = r < it.n_rows;
         if (valid) ri = item_row(p, it, r);
 #pragma unroll 4
@@ -445,22 +473,30 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
     tc::fence_after();
     const uint32_t tmem = sm.tmem_base;
 
-    if (warp == 0) {
-        if (lane == 0) producer(p, sm, it, ch, T);
-    } else if (warp == 1) {
-        if (lane == 0) mma_issuer(sm, tmem, T, MT);
-        __syncwarp();
-    } else if (warp >= 4) {
-        const int m = (warp - 4) >> 2;
-        if (m < MT) softmax(p, sm, ch, ri, valid, tmem, T, m, warp & 3, lane);
+    // Each role ends the kernel in its own branch: code after a register re-split must not
+    // be shared by warps with different register counts.
+    if (warp < 4) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kLowRegs));
+        if (warp == 0) {
+            producer<false>(p, sm, it, ch, T, lane);
+        } else if (warp == 1) {
+            mma_issuer(sm, tmem, T, MT, lane);
+        } else if (warp == 2) {
+            producer<true>(p, sm, it, ch, T, lane);
+        }
+        tc::fence_before();
+        __syncthreads();
+        if (warp == 1) {
+            tc::fence_after();
+            tc::tmem_dealloc(tmem, kTmemCols);
+        }
+        if (tid == 0 && sm.abort) atomicOr(p.err, kErrTimeout);
+    } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kHighRegs));
+        if (sm_m < MT) softmax(p, sm, ch, ri, valid, tmem, T, sm_m, warp & 3, lane);
+        tc::fence_before();
+        __syncthreads();
     }
-    tc::fence_before();
-    __syncthreads();
-    if (warp == 1) {
-        tc::fence_after();
-        tc::tmem_dealloc(tmem, kTmemCols);
-    }
-    if (tid == 0 && sm.abort) atomicOr(p.err, kErrTimeout);
 }
 
 }  // namespace tck
