@@ -14,8 +14,8 @@
 //                        K ring, warp 2 the 8 pages of V as whole 4 KiB page boxes into a
 //                        3-stage V ring; pages past the chunk's end are read at an
 //                        out-of-range page index, which the copy fills with zeros;
-//   warp 1               MMA issuer (one lane issues, the warp waits converged); the
-//                        whole warp allocates the 512 TMEM columns:
+//   warps 1 and 3        MMA issuers for M tile 0 and 1 (one lane issues, the warp waits
+//                        converged); warp 1 allocates the 512 TMEM columns:
 //                        O0 [0,128) O1 [128,256) S0/P0 [256,384) S1/P1 [384,512);
 //   warps 4-7, 8-11      softmax of M tile 0 and 1 (one row per thread, TMEM lane = row):
 //                        S from TMEM, mask (visibility words, chunk end, causal limit), base-2
@@ -170,9 +170,13 @@ __device__ __forceinline__ void producer(const DecodeParams &p, Smem &sm, const 
         wait_bar(ptx::smem_u32(kIsV ? &sm.vfull[j % NS] : &sm.kfull[j % NS]), (j / NS) & 1, &never);
 }
 
-// MMA warp: every lane waits on the barriers (the warp stays converged); lane 0 issues the
-// MMAs and the commits.
-__device__ __forceinline__ void mma_issuer(Smem &sm, uint32_t tmem, int T, int MT, int lane) {
+// MMA warps: warp 1 issues the MMAs of M tile 0, warp 3 those of M tile 1, so that one
+// warp's barrier waits and commits overlap the other's MMAs on the tensor core.  Every lane
+// waits on the barriers (the warp stays converged); lane 0 issues the MMAs and commits.  The
+// two sequences share no TMEM columns; the K/V stage-free barriers take one arrival per M
+// tile.  Per tile j: O_m (+)= P_m(j-1) V_(j-1), then S_m = Q_m K_j^T (S_m aliases P_m, so
+// it follows the P V that reads P_m).
+__device__ __forceinline__ void mma_issuer(Smem &sm, uint32_t tmem, int T, int m, int lane) {
     const volatile int32_t *abort = &sm.abort;
     const uint32_t qa = ptx::smem_u32(sm.q);
     bool ok = true;
@@ -180,63 +184,58 @@ __device__ __forceinline__ void mma_issuer(Smem &sm, uint32_t tmem, int T, int M
         ok = __all_sync(0xffffffffu, wait_bar(ptx::smem_u32(&bar), parity, abort));
         return ok;
     };
-    auto pv = [&](int m, int j) {  // O_m (+)= P_m V_j
-        if (lane == 0) {
-            const uint32_t vb = ptx::smem_u32(sm.v[j % kVStages]);
+    auto commit = [&](uint64_t &bar) {
+        if (lane == 0) tc::commit(ptx::smem_u32(&bar));
+        __syncwarp();
+    };
+    // descriptors are warp-uniform values computed by every lane; one elected lane issues
+    const uint64_t qdesc0 = tc::sdesc_sw128(qa + m * (kQHalf / 2), 16, 1024);
+    auto pv_issue = [&](int j) {  // O_m (+)= P_m V_j, then release V_j
+        const uint64_t vdesc = tc::sdesc_sw128(ptx::smem_u32(sm.v[j % kVStages]), 2048, 1024);
+        const uint32_t d = tmem + kColO + 128 * m, a = tmem + kColS + 128 * m;
+        if (tc::elect_one()) {
 #pragma unroll
-            for (int kk = 0; kk < kTilePages; ++kk)
-                tc::mma_ts(tmem + kColO + 128 * m, tmem + kColS + 128 * m + 8 * kk,
-                           tc::sdesc_sw128(vb + kk * 4096, 2048, 1024), kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < kTilePages; ++kk)  // +4 KiB per page: (4096 >> 4) in the address field
+                tc::mma_ts(d, a + 8 * kk, vdesc + uint64_t(kk * (4096 >> 4)), kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
             tc::commit(ptx::smem_u32(&sm.odone[m]));
+            tc::commit(ptx::smem_u32(&sm.vfree[j % kVStages]));
         }
         __syncwarp();
     };
-    auto qk = [&](int m, int j) {  // S_m = Q_m K_j^T
-        if (lane == 0) {
-            const uint32_t kb = ptx::smem_u32(sm.k[j % kKStages]);
+    auto qk = [&](int j) {  // S_m = Q_m K_j^T, then release K_j
+        const uint64_t kdesc = tc::sdesc_sw128(ptx::smem_u32(sm.k[j % kKStages]), 16, 1024);
+        const uint32_t d = tmem + kColS + 128 * m;
+        if (tc::elect_one()) {
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
-                const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-                tc::mma_ss(tmem + kColS + 128 * m,
-                           tc::sdesc_sw128(qa + (kk >> 2) * kQHalf + m * (kQHalf / 2) + (kk & 3) * 32, 16, 1024),
-                           tc::sdesc_sw128(kb + off, 16, 1024), kIdescQK, kk > 0 ? 1u : 0u);
+                // K step kk: dims 16 kk .. 16 kk + 15 = half kk / 4, 32-byte column kk % 4
+                const uint64_t qoff = uint64_t(((kk >> 2) * kQHalf + (kk & 3) * 32) >> 4);
+                const uint64_t koff = uint64_t(((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4);
+                tc::mma_ss(d, qdesc0 + qoff, kdesc + koff, kIdescQK, kk > 0 ? 1u : 0u);
             }
             tc::commit(ptx::smem_u32(&sm.sfull[m]));
+            tc::commit(ptx::smem_u32(&sm.kfree[j % kKStages]));
         }
         __syncwarp();
     };
-    for (int j = 0; j < T && ok; ++j) {
-        for (int m = 0; m < MT && ok; ++m) {
-            if (j > 0) {
-                if (m == 0 && !wait(sm.vfull[(j - 1) % kVStages], ((j - 1) / kVStages) & 1)) break;
-                if (!wait(sm.pfull[m], (j - 1) & 1)) break;
-                tc::fence_after();
-                pv(m, j - 1);
-            }
-            if (m == 0) {
-                if (!wait(sm.kfull[j % kKStages], (j / kKStages) & 1)) break;
-                tc::fence_after();
-            }
-            qk(m, j);
-        }
-        if (!ok) break;
-        if (lane == 0) {
-            tc::commit(ptx::smem_u32(&sm.kfree[j % kKStages]));
-            if (j > 0) tc::commit(ptx::smem_u32(&sm.vfree[(j - 1) % kVStages]));
-        }
-        __syncwarp();
+    auto pv = [&](int j) {
+        if (!wait(sm.vfull[j % kVStages], (j / kVStages) & 1)) return false;
+        if (!wait(sm.pfull[m], j & 1)) return false;
+        tc::fence_after();
+        pv_issue(j);
+        return true;
+    };
+    for (int j = 0; j < T; ++j) {
+        if (j > 0 && !pv(j - 1)) break;
+        if (!wait(sm.kfull[j % kKStages], (j / kKStages) & 1)) break;
+        tc::fence_after();
+        qk(j);
     }
-    if (ok && wait(sm.vfull[(T - 1) % kVStages], ((T - 1) / kVStages) & 1)) {
-        for (int m = 0; m < MT; ++m) {
-            if (!wait(sm.pfull[m], (T - 1) & 1)) break;
-            tc::fence_after();
-            pv(m, T - 1);
-        }
-    }
+    if (ok) pv(T - 1);
     if (!ok && lane == 0) *reinterpret_cast<volatile int32_t *>(&sm.abort) = 1;
-    // all MMAs issued by this warp are complete before TMEM is freed
-    if (lane == 0) tc::commit(ptx::smem_u32(&sm.fin));
-    __syncwarp();
+    // all MMAs issued by either MMA warp are complete before TMEM is freed (fin takes one
+    // arrival per M tile)
+    commit(sm.fin);
     const volatile int32_t never = 0;
     wait_bar(ptx::smem_u32(&sm.fin), 0, &never);
 }
@@ -431,18 +430,18 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
     if (tid == 0) {
         for (int s = 0; s < kKStages; ++s) {
             ptx::mbar_init(ptx::smem_u32(&sm.kfull[s]), 1);
-            ptx::mbar_init(ptx::smem_u32(&sm.kfree[s]), 1);
+            ptx::mbar_init(ptx::smem_u32(&sm.kfree[s]), MT);  // one arrival per MMA warp
         }
         for (int s = 0; s < kVStages; ++s) {
             ptx::mbar_init(ptx::smem_u32(&sm.vfull[s]), 1);
-            ptx::mbar_init(ptx::smem_u32(&sm.vfree[s]), 1);
+            ptx::mbar_init(ptx::smem_u32(&sm.vfree[s]), MT);
         }
         for (int m = 0; m < 2; ++m) {
             ptx::mbar_init(ptx::smem_u32(&sm.sfull[m]), 1);
             ptx::mbar_init(ptx::smem_u32(&sm.pfull[m]), 128);
             ptx::mbar_init(ptx::smem_u32(&sm.odone[m]), 1);
         }
-        ptx::mbar_init(ptx::smem_u32(&sm.fin), 1);
+        ptx::mbar_init(ptx::smem_u32(&sm.fin), MT);
         sm.abort = 0;
         ptx::fence_mbar_init();
     }
@@ -480,7 +479,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
         if (warp == 0) {
             producer<false>(p, sm, it, ch, T, lane);
         } else if (warp == 1) {
-            mma_issuer(sm, tmem, T, MT, lane);
+            mma_issuer(sm, tmem, T, 0, lane);
+        } else if (warp == 3) {
+            if (MT > 1) mma_issuer(sm, tmem, T, 1, lane);
         } else if (warp == 2) {
             producer<true>(p, sm, it, ch, T, lane);
         }
