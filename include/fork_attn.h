@@ -180,9 +180,14 @@ int fork_attn_decode(const void *q, const void *k_pages, const void *v_pages,
                      const fa_plan *plan, void *out, float *lse, void *stream);
 
 /* Like fork_attn_decode; if `events` [host] is not NULL it is an array of 2*n_events
- * cudaEvent_t handles (as void*) recorded on `stream` around each kernel launch, in launch
- * order: [start_0, stop_0, start_1, stop_1, ...] for the row kernel, the tcgen05 kernel and
- * the merge kernel (an absent kernel records start = stop).  n_events must be 0 or 3. */
+ * cudaEvent_t handles (as void*) recorded around each kernel launch on the stream that
+ * kernel runs on: [start_0, stop_0, start_1, stop_1, start_2, stop_2] for the row kernel,
+ * the tcgen05 kernel and the merge kernel (an absent kernel records start = stop).  When a
+ * plan has work for both the row and the tcgen05 kernel, fork_attn_decode runs the row
+ * kernel on a library-owned helper stream of the current device (created on the device's
+ * first such decode) concurrently with the tcgen05 kernel on `stream`, joined by events
+ * before the merge; the whole decode stays ordered on `stream` and capturable in a CUDA
+ * graph.  n_events must be 0 or 3. */
 int fork_attn_decode_timed(const void *q, const void *k_pages, const void *v_pages,
                            const fa_plan *plan, void *out, float *lse, void *stream,
                            void **events, int32_t n_events);

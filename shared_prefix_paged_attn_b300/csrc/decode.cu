@@ -131,26 +131,68 @@ int fill_params(const fa_plan *plan, const void *q, const void *k_pages, const v
 
 bool needs_merge(const fa_plan *plan) { return plan->stats.merge_rows > 0; }
 
-int launch_all(const fa::DecodeParams &p, const fa_plan *plan, cudaStream_t st, void **events) {
+// Per-device helper stream and events that let the row kernel and the tcgen05 kernel run at
+// the same time (each fills the SMs the other's last wave leaves idle).  Created on a
+// device's first concurrent decode; the fork/join is plain stream work (event record +
+// stream wait), so a decode can be captured into a CUDA graph.
+struct Aux {
+    cudaStream_t stream = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+    std::mutex mu;  // the two events are shared by every decode on the device
+};
+
+Aux *aux_for_current_device() {
+    static std::mutex mu;
+    static Aux aux[128];
+    static bool ready[128] = {false};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return nullptr;
+    std::lock_guard<std::mutex> lk(mu);
+    if (!ready[dev]) {
+        if (cudaStreamCreateWithFlags(&aux[dev].stream, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaEventCreateWithFlags(&aux[dev].fork, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&aux[dev].join, cudaEventDisableTiming) != cudaSuccess)
+            return nullptr;
+        ready[dev] = true;
+    }
+    return &aux[dev];
+}
+
+// Launches the decode kernels on `st`.  With `aux`, the row kernel runs on the helper stream
+// concurrently with the tcgen05 kernel, and the merge waits for both.  `events` (optional)
+// are recorded around each kernel on the stream it runs on.
+int launch_all(const fa::DecodeParams &p, const fa_plan *plan, cudaStream_t st, void **events, Aux *aux) {
     bool ev_ok = true;
-    auto rec = [&](int i) {
-        if (events) ev_ok = ev_ok && cudaEventRecord(static_cast<cudaEvent_t>(events[i]), st) == cudaSuccess;
+    auto rec = [&](int i, cudaStream_t s) {
+        if (events) ev_ok = ev_ok && cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s) == cudaSuccess;
     };
-    rec(0);
-    if (p.n_items > 0)
-        fa::rowk::row_kernel<<<p.n_items, fa::rowk::kThreads, fa::rowk::kSmemBytes, st>>>(p);
-    rec(1);
-    rec(2);
+    const bool both = aux && p.n_items > 0 && p.n_items_tc > 0;
+    std::unique_lock<std::mutex> lk;
+    if (both) {
+        lk = std::unique_lock<std::mutex>(aux->mu);
+        if (cudaEventRecord(aux->fork, st) != cudaSuccess || cudaStreamWaitEvent(aux->stream, aux->fork, 0) != cudaSuccess)
+            return FA_ERR_CUDA;
+    }
+    cudaStream_t rs = both ? aux->stream : st;
+    rec(2, st);
     if (p.n_items_tc > 0)
         fa::tck::tc_kernel<<<p.n_items_tc, fa::tck::kThreads, fa::tck::kSmemBytes, st>>>(p);
-    rec(3);
-    rec(4);
+    rec(3, st);
+    rec(0, rs);
+    if (p.n_items > 0)
+        fa::rowk::row_kernel<<<p.n_items, fa::rowk::kThreads, fa::rowk::kSmemBytes, rs>>>(p);
+    rec(1, rs);
+    if (both) {
+        if (cudaEventRecord(aux->join, aux->stream) != cudaSuccess || cudaStreamWaitEvent(st, aux->join, 0) != cudaSuccess)
+            return FA_ERR_CUDA;
+    }
+    rec(4, st);
     if (needs_merge(plan)) {
         const int64_t threads = int64_t(p.total_rows) * 32;
         const int blocks = int((threads + fa::mergek::kThreads - 1) / fa::mergek::kThreads);
         fa::mergek::merge_kernel<<<blocks, fa::mergek::kThreads, 0, st>>>(p);
     }
-    rec(5);
+    rec(5, st);
     const bool launched = cudaGetLastError() == cudaSuccess;
     if (!ev_ok) return FA_ERR_INVALID;
     return launched ? FA_OK : FA_ERR_CUDA;
@@ -193,7 +235,9 @@ extern "C" int fork_attn_decode_timed(const void *q, const void *k_pages, const 
     fa::DecodeParams p;
     rc = fill_params(plan, q, k_pages, v_pages, out, lse, plan->dev_scratch, p);
     if (rc != FA_OK) return rc;
-    return launch_all(p, plan, static_cast<cudaStream_t>(stream), events);
+    Aux *aux = aux_for_current_device();
+    if (!aux) return FA_ERR_CUDA;
+    return launch_all(p, plan, static_cast<cudaStream_t>(stream), events, aux);
 }
 
 extern "C" int fork_attn_decode(const void *q, const void *k_pages, const void *v_pages,
@@ -280,5 +324,5 @@ extern "C" int fork_attn_decode_static_scratch(const void *q, const void *k_page
     p.merge_bases = reinterpret_cast<const int32_t *>(base + L.merge_bases);
     p.mask_words = reinterpret_cast<const uint32_t *>(base + L.mask_words);
     p.err = reinterpret_cast<int32_t *>(base);
-    return launch_all(p, plan, st, nullptr);
+    return launch_all(p, plan, st, nullptr, nullptr);  // one stream: nothing is created here
 }

@@ -7,7 +7,7 @@
 //     L = max_k lse_k + ln sum_k exp(lse_k - max_k lse_k),    O = sum_k exp(lse_k - L) O_k.
 // One warp per row; each lane owns 4 of the 128 dims.  The partials' lse values are spread
 // over the lanes (max and weights by shuffles); the O terms are summed in the plan's fixed
-// order, four loads in flight at a time, so the result is bitwise run-to-run deterministic.
+// order, eight loads in flight at a time, so the result is bitwise run-to-run deterministic.
 #pragma once
 #include "decode_params.cuh"
 #include "ptx.cuh"
@@ -49,20 +49,20 @@ __global__ void __launch_bounds__(kThreads) merge_kernel(const __grid_constant__
             }
             // L in a fixed order: lane sums are added serially below, like the O terms
             int k = 0;
-            for (; k + 4 <= kn; k += 4) {
-                float w[4];
-                int r[4];
-                float4 v[4];
+            for (; k + 8 <= kn; k += 8) {
+                float w[8];
+                int r[8];
+                float4 v[8];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
+                for (int u = 0; u < 8; ++u) {
                     w[u] = __shfl_sync(0xffffffffu, wl, k + u);
                     r[u] = __shfl_sync(0xffffffffu, pr, k + u);
                 }
 #pragma unroll
-                for (int u = 0; u < 4; ++u)
+                for (int u = 0; u < 8; ++u)
                     v[u] = *reinterpret_cast<const float4 *>(p.part_o + size_t(r[u]) * kHeadDim + lane * 4);
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
+                for (int u = 0; u < 8; ++u) {
                     L += w[u];
                     acc.x += w[u] * v[u].x; acc.y += w[u] * v[u].y;
                     acc.z += w[u] * v[u].z; acc.w += w[u] * v[u].w;

@@ -385,6 +385,14 @@ int build_plan(Input &in, const fa_plan_opts &opts, fa_plan *plan) {
         if (em.rows.size() > size_t(INT32_MAX)) return FA_ERR_UNSUPPORTED;
     }
 
+    // longest chunks first (stable, so a chunk's row groups and heads stay adjacent and share
+    // its pages in L2): the last wave of CTAs is made of short items
+    auto by_len = [&](const fa::Item &a, const fa::Item &b) {
+        return em.chunks[a.chunk].n_pages > em.chunks[b.chunk].n_pages;
+    };
+    std::stable_sort(em.items_tc.begin(), em.items_tc.end(), by_len);
+    std::stable_sort(em.items_rows.begin(), em.items_rows.end(), by_len);
+
     st.num_chunks = int64_t(em.chunks.size());
     st.num_items_rows = int64_t(em.items_rows.size());
     st.num_items_tensor = int64_t(em.items_tc.size());
