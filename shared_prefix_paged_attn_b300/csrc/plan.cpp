@@ -13,8 +13,9 @@
 //      bits of that page for that reader (slot in the segment and not dropped);
 //   3. group records by physical page: a page's reader set is all of its records;
 //   4. chain pages into runs: page p' follows p when every reader of p reads p' at the next
-//      16 logical positions and nobody else reads p' (equal reader sets); pages that no
-//      reader sees at all are skipped, and end a run;
+//      16 logical positions and nobody else reads p' (equal reader sets), or, for pages that
+//      lie before every reader's query tokens, when the same readers read p' further on;
+//      pages that no reader sees at all are skipped;
 //   5. cut runs into chunks (long enough that fp32 partial results stay a few percent of the
 //      KV bytes, short enough for occupancy), pack per-reader visibility words, give every
 //      (chunk, reader) its partial rows (or a direct write when it is the branch's only one);
@@ -185,6 +186,35 @@ struct Builder {
         return true;
     }
 
+    // Every reader of page group g sees all of the page before its branch's first query token:
+    // no causal cut can fall inside it.
+    bool pre_query(int32_t g) const {
+        for (int32_t t = 0; t < group_count[g]; ++t) {
+            const Rec &a = recs[by_page[group_start[g] + t]];
+            const int64_t qpos0 = in.n_b[a.branch] - (in.q_off[a.branch + 1] - in.q_off[a.branch]);
+            if (int64_t(a.lpos0) + kPageSize > qpos0) return false;
+        }
+        return true;
+    }
+
+    // p1 may join p0's run although not logically adjacent: the same readers, each reading p1
+    // entirely after p0 (their order is kept) and entirely before its queries.
+    bool jumps(int32_t g0, int32_t g1) const {
+        if (group_count[g0] != group_count[g1]) return false;
+        for (int32_t t = 0; t < group_count[g0]; ++t) {
+            const Rec &a = recs[by_page[group_start[g0] + t]];
+            const Rec &b = recs[by_page[group_start[g1] + t]];
+            if (a.branch != b.branch || int64_t(b.lpos0) < int64_t(a.lpos0) + kPageSize) return false;
+        }
+        return pre_query(g1);
+    }
+
+    // Runs follow one branch's pages in logical order.  A page joins the run when every
+    // reader reads it right after the previous one, or -- while the whole run lies before
+    // every reader's queries -- when it has the same readers further on (attention over such
+    // tokens does not depend on their order or position, so a chunk may gather the visible
+    // pieces around dropped ones; the kernels' causal test then never cuts it).  Pages nobody
+    // sees are skipped.
     std::vector<std::vector<int32_t>> build_runs() {
         std::vector<std::vector<int32_t>> runs;
         std::vector<char> assigned(group_start.size(), 0);
@@ -195,15 +225,27 @@ struct Builder {
                 assigned[g] = 1;
                 if (group_union[g] == 0) continue;  // no reader sees this page: never read it
                 std::vector<int32_t> run{g};
+                bool all_pre = pre_query(g), jumped = false;
                 int64_t cur = r;
-                while (cur + 1 < branch_rec[b + 1]) {
-                    const Rec &nx = recs[cur + 1];
-                    if (int64_t(nx.lpos0) != int64_t(recs[cur].lpos0) + kPageSize) break;
+                for (int64_t nx_i = r + 1; nx_i < branch_rec[b + 1]; ++nx_i) {
+                    const Rec &nx = recs[nx_i];
                     const int32_t g1 = group_of_page[nx.page];
-                    if (assigned[g1] || group_union[g1] == 0 || !chains(run.back(), g1)) break;
+                    if (group_union[g1] == 0) continue;  // unseen pages leave no gap in a chunk
+                    if (assigned[g1]) break;
+                    const bool adjacent = int64_t(nx.lpos0) == int64_t(recs[cur].lpos0) + kPageSize &&
+                                          nx_i == cur + 1 && chains(run.back(), g1);
+                    const bool pre1 = pre_query(g1);
+                    if (adjacent && (!jumped || pre1)) {
+                        // plain continuation
+                    } else if (all_pre && jumps(run.back(), g1)) {
+                        jumped = true;
+                    } else {
+                        break;
+                    }
+                    all_pre = all_pre && pre1;
                     assigned[g1] = 1;
                     run.push_back(g1);
-                    ++cur;
+                    cur = nx_i;
                 }
                 runs.push_back(std::move(run));
             }
@@ -231,7 +273,7 @@ int build_plan(Input &in, const fa_plan_opts &opts, fa_plan *plan) {
 
     const fa_desc *s = in.s;
     const int32_t B = s->num_branches, G = in.G, Hkv = in.d->num_kv_heads;
-    const int32_t base_pages = opts.chunk_pages > 0 ? opts.chunk_pages : 32;
+    const int32_t base_pages = opts.chunk_pages > 0 ? opts.chunk_pages : 64;
     Emit em;
     fa_plan_stats &st = plan->stats;
     std::memset(&st, 0, sizeof st);
