@@ -31,6 +31,7 @@ from shared_prefix_paged_attn_b300 import workloads as W  # noqa: E402
 METRIC = "fork decode attention: unique-KV HBM GB/s (% of peak), branch-queries/sec"
 KV_BYTES_PER_SLOT_HEAD = 2 * 128 * 2  # K + V, bf16
 FALLBACK_HBM_GBS = 6400.0
+FALLBACK_BF16_TFLOPS = 1800.0
 
 
 def peaks():
@@ -39,6 +40,46 @@ def peaks():
         d = json.load(open(path))
         return float(d["hbm_gbs"]), "measured"
     return FALLBACK_HBM_GBS, "fallback"
+
+
+def tensor_peak():
+    """Dense bf16 tensor peak (TFLOP/s): the burst cuBLAS figure, since each kernel is timed per
+    launch within a sub-second loop."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return float(d["bf16_tflops"]), "measured (burst)"
+    return FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def kernel_source_hash():
+    """Short hash of the kernel sources: DRAM traffic read from an ncu capture only counts for the
+    kernels it was taken on."""
+    import hashlib
+    csrc = os.path.join(ROOT, "shared_prefix_paged_attn_b300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + b"\0" + fh.read())
+    return h.hexdigest()[:12]
+
+
+def ncu_traffic(workload):
+    """Per-launch DRAM bytes (read + write) of each kernel from profiles/ncu_traffic.md, rows
+    `| kernel | workload | source hash | bytes |`; only rows whose hash matches these sources."""
+    out = {}
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.md")
+    if not os.path.exists(path):
+        return out
+    want = kernel_source_hash()
+    for line in open(path):
+        f = [x.strip() for x in line.strip().strip("|").split("|")]
+        if len(f) >= 4 and f[1] == workload and f[2] == want:
+            try:
+                out[f[0]] = int(f[3])
+            except ValueError:
+                pass
+    return out
 
 
 class ClockSampler:
@@ -236,7 +277,6 @@ def run_ours(args):
     K = args.steps
     ev_start = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     ev_stop = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
     if dist:
         dist.barrier()
     torch.cuda.synchronize(dev)
@@ -245,14 +285,13 @@ def run_ours(args):
         for i in range(K):
             flush.zero_()
             ev_start[i].record(stream)
-            step(kev[i])
+            step()
             ev_stop[i].record(stream)
         torch.cuda.synchronize(dev)
     wall = time.perf_counter() - wall0
     if dist:
         dist.barrier()
     step_ms = [a.elapsed_time(b) for a, b in zip(ev_start, ev_stop)]
-    kern_ms = [[kev[i][2 * j].elapsed_time(kev[i][2 * j + 1]) for i in range(K)] for j in range(3)]
     assert fa.fork_attn_check(run.plan, stream) == 0, "device error word set in the timed region"
     ms = sum(step_ms) / K
     ms_max = ms
@@ -263,13 +302,43 @@ def run_ours(args):
     value = unique_bytes * world / (ms_max * 1e-3) / 1e9
     bq_s = w.total_q * world / (ms_max * 1e-3)
 
-    # dominant kernel and its roofline (algorithmic bytes = unique visible slots it reads)
+    # Per-kernel durations: the decode's kernels overlap in the timed region (the row kernel
+    # runs on a helper stream beside the tcgen05 kernel), so each kernel is timed alone in a
+    # second pass of the same decode with its kernels run one after another
+    # (fork_attn_decode_timed), L2 flushed before every step as above.
+    Kk = min(K, 200)
+    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(Kk)]
+    for i in range(Kk):
+        flush.zero_()
+        step(kev[i])
+    torch.cuda.synchronize(dev)
+    assert fa.fork_attn_check(run.plan, stream) == 0, "device error word set in the per-kernel pass"
+    kern_ms = [[kev[i][2 * j].elapsed_time(kev[i][2 * j + 1]) for i in range(Kk)] for j in range(3)]
     names = ["row_kernel", "tcgen05_kernel", "merge_kernel"]
-    avg = [sum(x) / K for x in kern_ms]
-    dom = int(np.argmax(avg))
-    alg = {0: st["unique_slots_rows"], 1: st["unique_slots_tensor"]}.get(dom, 0) * w.num_kv_heads * KV_BYTES_PER_SLOT_HEAD
-    peak, peak_kind = peaks()
-    achieved = alg / (avg[dom] * 1e-3) / 1e9 if avg[dom] > 0 else 0.0
+    avg = [sum(x) / Kk for x in kern_ms]
+    hbm_peak, peak_kind = peaks()
+    tflops_peak, tpeak_kind = tensor_peak()
+    traffic = ncu_traffic(w.name)
+    part_bytes = st["partial_rows"] * (128 * 4 + 4) * 2  # fp32 partial O + lse, written then read
+    kernels = {}
+    for j, n in enumerate(names):
+        if avg[j] <= 0:
+            continue
+        if n == "tcgen05_kernel":
+            ach = st["flops_tensor"] / (avg[j] * 1e-3) / 1e12
+            kernels[n] = {"bound": "tensor", "achieved": ach, "peak": tflops_peak, "unit": "TFLOP/s",
+                          "frac": ach / tflops_peak, "ms": avg[j], "peak_kind": tpeak_kind,
+                          "algorithmic": st["flops_tensor"], "traffic": traffic.get(n)}
+        else:
+            alg = (st["unique_slots_rows"] * w.num_kv_heads * KV_BYTES_PER_SLOT_HEAD if n == "row_kernel"
+                   else part_bytes // 2 + st["merge_rows"] * (128 * 2 + 4))
+            ach = alg / (avg[j] * 1e-3) / 1e9
+            kernels[n] = {"bound": "hbm", "achieved": ach, "peak": hbm_peak, "unit": "GB/s",
+                          "frac": ach / hbm_peak, "ms": avg[j], "peak_kind": peak_kind,
+                          "algorithmic": alg, "traffic": traffic.get(n)}
+    dom = max(kernels, key=lambda n: kernels[n]["ms"])
+    roof = dict(kernels[dom])
+    roof["kernel"] = dom
 
     e2e = None
     if not args.no_e2e and rank == 0:
@@ -320,15 +389,16 @@ def run_ours(args):
                        "unique_kv_bytes": unique_bytes, "l2": "flushed (256 MiB write) between steps",
                        "plan_s": plan_s},
             "branch_queries_per_s": bq_s,
-            "frac_of_hbm_peak": value / world / peak,
-            "roofline": {"bound": "hbm", "kernel": names[dom], "achieved": achieved, "peak": peak,
-                         "unit": "GB/s", "frac": achieved / peak, "traffic": None,
-                         "peak_kind": peak_kind},
+            "frac_of_hbm_peak": value / world / hbm_peak,
+            "roofline": roof,
+            "kernels": kernels,
             "kernel_ms": {n: a for n, a in zip(names, avg)},
+            "per_kernel_pass": f"{Kk} steps, kernels run one after another (fork_attn_decode_timed)",
             "step_ms_min": min(step_ms), "step_ms_median": statistics.median(step_ms),
             "wall_s_timed_region": wall,
             "gpu_launches": K * (int(st["num_items_rows"] > 0) + int(st["num_items_tensor"] > 0)
                                  + int(st["merge_rows"] > 0)),
+            "flops_per_step": st["flops_rows"] + st["flops_tensor"],
             "clocks": clk.record(),
             "e2e": e2e,
             "cpu_baseline": cpu,

@@ -137,7 +137,9 @@ typedef struct {
     int64_t total_q;
     int64_t unique_slots_rows;     /* distinct visible physical slots read by the row kernel */
     int64_t unique_slots_tensor;   /* distinct visible physical slots read by tcgen05 kernel */
-    int64_t reserved[3];
+    int64_t flops_rows;            /* algorithmic flops of the row kernel: per visible slot  */
+    int64_t flops_tensor;          /* of a reader, 4 x 128 x (query rows) per KV head        */
+    int64_t reserved[1];
 } fa_plan_stats;
 
 typedef struct fa_plan fa_plan; /* opaque; owned by the library */
@@ -179,15 +181,17 @@ int fork_attn_plan_upload(fa_plan *plan, void *dev_plan_buf, size_t plan_buf_byt
 int fork_attn_decode(const void *q, const void *k_pages, const void *v_pages,
                      const fa_plan *plan, void *out, float *lse, void *stream);
 
-/* Like fork_attn_decode; if `events` [host] is not NULL it is an array of 2*n_events
- * cudaEvent_t handles (as void*) recorded around each kernel launch on the stream that
- * kernel runs on: [start_0, stop_0, start_1, stop_1, start_2, stop_2] for the row kernel,
- * the tcgen05 kernel and the merge kernel (an absent kernel records start = stop).  When a
- * plan has work for both the row and the tcgen05 kernel, fork_attn_decode runs the row
- * kernel on a library-owned helper stream of the current device (created on the device's
- * first such decode) concurrently with the tcgen05 kernel on `stream`, joined by events
- * before the merge; the whole decode stays ordered on `stream` and capturable in a CUDA
- * graph.  n_events must be 0 or 3. */
+/* The same decode with its three kernels run one after the other on `stream` (no helper
+ * stream), for timing each kernel alone: if `events` [host] is not NULL it is an array of
+ * 2*n_events cudaEvent_t handles (as void*) recorded on `stream` around each kernel launch:
+ * [start_0, stop_0, start_1, stop_1, start_2, stop_2] for the row kernel, the tcgen05 kernel
+ * and the merge kernel (an absent kernel records start = stop).  n_events must be 0 or 3.
+ *
+ * (fork_attn_decode itself, when a plan has work for both the row and the tcgen05 kernel,
+ * runs the row kernel on a library-owned helper stream of the current device -- created on
+ * that device's first such decode -- concurrently with the tcgen05 kernel on `stream`; the
+ * two are joined by events before the merge, so the decode stays ordered on `stream` and
+ * can be captured in a CUDA graph.) */
 int fork_attn_decode_timed(const void *q, const void *k_pages, const void *v_pages,
                            const fa_plan *plan, void *out, float *lse, void *stream,
                            void **events, int32_t n_events);

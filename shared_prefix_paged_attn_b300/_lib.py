@@ -43,7 +43,8 @@ class FaPlanStats(ctypes.Structure):
                 ("kv_bytes_rows", c_int64), ("kv_bytes_tensor", c_int64),
                 ("partial_rows", c_int64), ("merge_rows", c_int64), ("total_q", c_int64),
                 ("unique_slots_rows", c_int64), ("unique_slots_tensor", c_int64),
-                ("reserved", c_int64 * 3)]
+                ("flops_rows", c_int64), ("flops_tensor", c_int64),
+                ("reserved", c_int64 * 1)]
 
 
 # name -> (restype, argtypes); every symbol declared in include/fork_attn.h

@@ -235,14 +235,24 @@ extern "C" int fork_attn_decode_timed(const void *q, const void *k_pages, const 
     fa::DecodeParams p;
     rc = fill_params(plan, q, k_pages, v_pages, out, lse, plan->dev_scratch, p);
     if (rc != FA_OK) return rc;
-    Aux *aux = aux_for_current_device();
-    if (!aux) return FA_ERR_CUDA;
-    return launch_all(p, plan, static_cast<cudaStream_t>(stream), events, aux);
+    return launch_all(p, plan, static_cast<cudaStream_t>(stream), events, nullptr);  // sequential
 }
 
 extern "C" int fork_attn_decode(const void *q, const void *k_pages, const void *v_pages,
                                 const fa_plan *plan, void *out, float *lse, void *stream) {
-    return fork_attn_decode_timed(q, k_pages, v_pages, plan, out, lse, stream, nullptr, 0);
+    if (!plan || !q || !k_pages || !v_pages || !out || !lse) return FA_ERR_NULL;
+    if (!plan->uploaded) return FA_ERR_NOT_UPLOADED;
+    if (!aligned(q, 16) || !aligned(k_pages, 16) || !aligned(v_pages, 16) || !aligned(out, 16) ||
+        !aligned(lse, 16))
+        return FA_ERR_ALIGN;
+    int rc = set_smem_attr();
+    if (rc != FA_OK) return rc;
+    fa::DecodeParams p;
+    rc = fill_params(plan, q, k_pages, v_pages, out, lse, plan->dev_scratch, p);
+    if (rc != FA_OK) return rc;
+    Aux *aux = aux_for_current_device();
+    if (!aux) return FA_ERR_CUDA;
+    return launch_all(p, plan, static_cast<cudaStream_t>(stream), nullptr, aux);
 }
 
 extern "C" int fork_attn_check(fa_plan *plan, int32_t *device_error, void *stream) {

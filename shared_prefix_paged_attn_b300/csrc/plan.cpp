@@ -313,8 +313,15 @@ int build_plan(Input &in, const fa_plan_opts &opts, fa_plan *plan) {
                 st.unique_visible_slots += __builtin_popcount(bd.group_union[g]);
                 (tc_run ? st.unique_slots_tensor : st.unique_slots_rows) += __builtin_popcount(bd.group_union[g]);
                 st.touched_pages += 1;
-                for (int32_t t = 0; t < n_read; ++t)
-                    st.listed_visible_slots += __builtin_popcount(bd.recs[bd.by_page[bd.group_start[g] + t]].vis);
+                for (int32_t t = 0; t < n_read; ++t) {
+                    const Rec &rd = bd.recs[bd.by_page[bd.group_start[g] + t]];
+                    const int64_t seen = __builtin_popcount(rd.vis);
+                    st.listed_visible_slots += seen;
+                    // QK^T and P V: 2 x 128 multiply-adds per visible slot, query row and KV head
+                    const int64_t fl = seen * int64_t(in.q_off[rd.branch + 1] - in.q_off[rd.branch]) * G * Hkv * 4 *
+                                       fa::kHeadDim;
+                    (tc_run ? st.flops_tensor : st.flops_rows) += fl;
+                }
             }
             for (int32_t t = 0; t < n_read; ++t) {
                 const Rec &rd = bd.recs[bd.by_page[bd.group_start[run[pos]] + t]];

@@ -122,3 +122,24 @@ def test_plan_is_deterministic():
     w = W.config3(shrink=16, values=False)
     a, b = fa.plan_for(w), fa.plan_for(w)
     assert a.sizes() == b.sizes() and a.stats() == b.stats()
+
+
+def _visible_positions(w, b):
+    n = w.branch_len(b)
+    if w.vis_bits is None:
+        return n
+    words = w.vis_bits[w.vis_word_off[b]:w.vis_word_off[b + 1]]
+    j = np.arange(n)
+    return int(((words[j // 32] >> (j % 32)) & 1).sum())
+
+
+@pytest.mark.parametrize("cfg", [1, 2, 3, 4, 5])
+def test_flop_counters_match_the_definition(cfg):
+    # QK^T and P V: 2 x 128 multiply-adds for every visible entry of every query row and KV head
+    w = W.make(cfg, small=True, values=False)
+    st = fa.plan_for(w).stats()
+    G = w.num_q_heads // w.num_kv_heads
+    want = sum(_visible_positions(w, b) * int(w.branch_q_off[b + 1] - w.branch_q_off[b])
+               for b in range(w.num_branches)) * G * w.num_kv_heads * 4 * 128
+    assert st["flops_rows"] + st["flops_tensor"] == want
+    assert st["flops_tensor"] > 0 or cfg == 1
