@@ -113,7 +113,7 @@ int fill_params(const fa_plan *plan, const void *q, const void *k_pages, const v
     p.items_tc = reinterpret_cast<const fa::Item *>(base + L.items_tc);
     p.rows = reinterpret_cast<const fa::RowRec *>(base + L.rows);
     p.branches = reinterpret_cast<const fa::Branch *>(base + L.branches);
-    p.q_branch = reinterpret_cast<const int32_t *>(base + L.q_branch);
+    p.q_merge = reinterpret_cast<const fa::QMerge *>(base + L.q_merge);
     p.merge_bases = reinterpret_cast<const int32_t *>(base + L.merge_bases);
     p.mask_words = reinterpret_cast<const uint32_t *>(base + L.mask_words);
     p.err = reinterpret_cast<int32_t *>(base);
@@ -330,7 +330,7 @@ extern "C" int fork_attn_decode_static_scratch(const void *q, const void *k_page
     p.items_tc = reinterpret_cast<const fa::Item *>(base + L.items_tc);
     p.rows = reinterpret_cast<const fa::RowRec *>(base + L.rows);
     p.branches = reinterpret_cast<const fa::Branch *>(base + L.branches);
-    p.q_branch = reinterpret_cast<const int32_t *>(base + L.q_branch);
+    p.q_merge = reinterpret_cast<const fa::QMerge *>(base + L.q_merge);
     p.merge_bases = reinterpret_cast<const int32_t *>(base + L.merge_bases);
     p.mask_words = reinterpret_cast<const uint32_t *>(base + L.mask_words);
     p.err = reinterpret_cast<int32_t *>(base);

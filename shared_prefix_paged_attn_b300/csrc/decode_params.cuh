@@ -23,7 +23,7 @@ struct DecodeParams {
     const Item *items_tc;  // tcgen05-kernel work items
     const RowRec *rows;
     const Branch *branches;
-    const int32_t *q_branch;
+    const QMerge *q_merge;
     const int32_t *merge_bases;
     const uint32_t *mask_words;
     int32_t *err;

@@ -5,9 +5,10 @@
 // branch's results are merged.  For a (query token, query head) row with partials
 // (O_k, lse_k) over disjoint sets of entries:
 //     L = max_k lse_k + ln sum_k exp(lse_k - max_k lse_k),    O = sum_k exp(lse_k - L) O_k.
-// One warp per row; each lane owns 4 of the 128 dims.  The partials' lse values are spread
-// over the lanes (max and weights by shuffles); the O terms are summed in the plan's fixed
-// order, eight loads in flight at a time, so the result is bitwise run-to-run deterministic.
+// One warp per row; each lane owns 4 of the 128 dims.  The row's merge record is one load;
+// the partials' lse values are spread over the lanes (max and weights by shuffles); the O
+// terms are summed in the plan's fixed order, eight loads in flight at a time, so the result
+// is bitwise run-to-run deterministic.
 #pragma once
 #include "decode_params.cuh"
 #include "ptx.cuh"
@@ -22,12 +23,12 @@ __global__ void __launch_bounds__(kThreads) merge_kernel(const __grid_constant__
     const int lane = threadIdx.x & 31;
     if (row >= p.total_rows) return;
     const int qt = row / p.Hq, h = row % p.Hq;
-    const Branch br = p.branches[p.q_branch[qt]];
-    if (br.direct) return;  // its only chunk wrote the output
-    const int i = qt - br.q_begin, g = h / p.G, jh = h % p.G;
-    const int off = (i * p.G + jh) * p.Hkv + g;
-    const int32_t *bases = p.merge_bases + br.merge_off;
-    const int n = br.n_merge;
+    const int4 qm = __ldg(reinterpret_cast<const int4 *>(p.q_merge) + qt);  // merge_off, n, direct, i
+    if (qm.z) return;  // its only chunk wrote the output
+    const int g = h / p.G, jh = h % p.G;
+    const int off = (qm.w * p.G + jh) * p.Hkv + g;
+    const int32_t *bases = p.merge_bases + qm.x;
+    const int n = qm.y;
 
     // partial k's lse sits in lane k % 32 (rounds of 32); max and weights by shuffles
     float M = -INFINITY;
@@ -47,7 +48,7 @@ __global__ void __launch_bounds__(kThreads) merge_kernel(const __grid_constant__
                 pr = bases[k0 + lane] + off;
                 wl = expf(p.part_lse[pr] - M);
             }
-            // L in a fixed order: lane sums are added serially below, like the O terms
+            // the O terms in the plan's order, eight loads in flight
             int k = 0;
             for (; k + 8 <= kn; k += 8) {
                 float w[8];

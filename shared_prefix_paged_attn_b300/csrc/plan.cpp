@@ -261,7 +261,8 @@ struct Emit {
     std::vector<fa::Item> items_rows, items_tc;
     std::vector<fa::RowRec> rows;
     std::vector<fa::Branch> branches;
-    std::vector<int32_t> q_branch, merge_bases;
+    std::vector<fa::QMerge> q_merge;
+    std::vector<int32_t> merge_bases;
     std::vector<uint32_t> mask_words;
 };
 
@@ -376,7 +377,7 @@ int build_plan(Input &in, const fa_plan_opts &opts, fa_plan *plan) {
         br.n_merge = int32_t(per_branch[b].size());
         br.direct = occ_count[b] == 1;
         em.merge_bases.insert(em.merge_bases.end(), per_branch[b].begin(), per_branch[b].end());
-        for (int32_t i = 0; i < br.n_q; ++i) em.q_branch.push_back(b);
+        for (int32_t i = 0; i < br.n_q; ++i) em.q_merge.push_back(fa::QMerge{br.merge_off, br.n_merge, br.direct, i});
         if (occ_count[b] != 1) st.merge_rows += int64_t(br.n_q) * in.d->num_q_heads;
     }
 
@@ -462,7 +463,7 @@ int build_plan(Input &in, const fa_plan_opts &opts, fa_plan *plan) {
     L.items_tc = place(int64_t(em.items_tc.size()) * sizeof(fa::Item));
     L.rows = place(int64_t(em.rows.size()) * sizeof(fa::RowRec));
     L.branches = place(int64_t(em.branches.size()) * sizeof(fa::Branch));
-    L.q_branch = place(int64_t(em.q_branch.size()) * 4);
+    L.q_merge = place(int64_t(em.q_merge.size()) * sizeof(fa::QMerge));
     L.merge_bases = place(int64_t(em.merge_bases.size()) * 4);
     L.mask_words = place(int64_t(em.mask_words.size()) * 4);
     L.total = off;
@@ -483,7 +484,7 @@ int build_plan(Input &in, const fa_plan_opts &opts, fa_plan *plan) {
     put(L.items_tc, em.items_tc.data(), em.items_tc.size() * sizeof(fa::Item));
     put(L.rows, em.rows.data(), em.rows.size() * sizeof(fa::RowRec));
     put(L.branches, em.branches.data(), em.branches.size() * sizeof(fa::Branch));
-    put(L.q_branch, em.q_branch.data(), em.q_branch.size() * 4);
+    put(L.q_merge, em.q_merge.data(), em.q_merge.size() * sizeof(fa::QMerge));
     put(L.merge_bases, em.merge_bases.data(), em.merge_bases.size() * 4);
     put(L.mask_words, em.mask_words.data(), em.mask_words.size() * 4);
     plan->partial_rows = prow;

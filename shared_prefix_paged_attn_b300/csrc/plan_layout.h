@@ -69,10 +69,20 @@ struct Branch {
     int32_t pad[2];
 };
 
+// Per query token, what the merge kernel needs: its branch's partial-row bases
+// merge_bases[merge_off .. merge_off + n_merge), whether its only chunk wrote `out` directly,
+// and its index i among the branch's query tokens.
+struct QMerge {
+    int32_t merge_off;
+    int32_t n_merge;
+    int32_t direct;
+    int32_t i;
+};
+
 // Byte offsets of the arrays inside the device plan buffer.  The first 256 bytes hold the
 // device error word (int32 at offset 0).
 struct Layout {
-    int64_t chunk_pages, chunks, items_rows, items_tc, rows, branches, q_branch, merge_bases,
+    int64_t chunk_pages, chunks, items_rows, items_tc, rows, branches, q_merge, merge_bases,
         mask_words, total;
     int32_t n_chunk_pages, n_chunks, n_items_rows, n_items_tc, n_rows, n_branches, total_q,
         n_merge_bases, n_mask_words;
