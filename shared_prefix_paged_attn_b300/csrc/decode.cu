@@ -131,14 +131,16 @@ int fill_params(const fa_plan *plan, const void *q, const void *k_pages, const v
 
 bool needs_merge(const fa_plan *plan) { return plan->stats.merge_rows > 0; }
 
-// Per-device helper stream and events that let the row kernel and the tcgen05 kernel run at
-// the same time (each fills the SMs the other's last wave leaves idle).  Created on a
-// device's first concurrent decode; the fork/join is plain stream work (event record +
-// stream wait), so a decode can be captured into a CUDA graph.
+// Per-device helper streams and events that let the row kernel and the tcgen05 kernel run at
+// the same time.  The tcgen05 kernel (one CTA per SM, the longer critical path) runs on the
+// highest-priority stream so that freed SMs take its CTAs first; the row kernel's CTAs fill
+// whatever is left.  Created on a device's first concurrent decode; the fork/join is plain
+// stream work (event record + stream wait), so a decode can be captured into a CUDA graph.
 struct Aux {
-    cudaStream_t stream = nullptr;
-    cudaEvent_t fork = nullptr, join = nullptr;
-    std::mutex mu;  // the two events are shared by every decode on the device
+    cudaStream_t tc_stream = nullptr;   // highest priority: the tcgen05 kernel's CTAs go first
+    cudaStream_t row_stream = nullptr;  // lowest priority: row CTAs fill the SMs left over
+    cudaEvent_t fork = nullptr, join_tc = nullptr, join_row = nullptr;
+    std::mutex mu;  // the events are shared by every decode on the device
 };
 
 Aux *aux_for_current_device() {
@@ -149,17 +151,21 @@ Aux *aux_for_current_device() {
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return nullptr;
     std::lock_guard<std::mutex> lk(mu);
     if (!ready[dev]) {
-        if (cudaStreamCreateWithFlags(&aux[dev].stream, cudaStreamNonBlocking) != cudaSuccess ||
+        int least = 0, greatest = 0;
+        if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess ||
+            cudaStreamCreateWithPriority(&aux[dev].tc_stream, cudaStreamNonBlocking, greatest) != cudaSuccess ||
+            cudaStreamCreateWithPriority(&aux[dev].row_stream, cudaStreamNonBlocking, least) != cudaSuccess ||
             cudaEventCreateWithFlags(&aux[dev].fork, cudaEventDisableTiming) != cudaSuccess ||
-            cudaEventCreateWithFlags(&aux[dev].join, cudaEventDisableTiming) != cudaSuccess)
+            cudaEventCreateWithFlags(&aux[dev].join_tc, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&aux[dev].join_row, cudaEventDisableTiming) != cudaSuccess)
             return nullptr;
         ready[dev] = true;
     }
     return &aux[dev];
 }
 
-// Launches the decode kernels on `st`.  With `aux`, the row kernel runs on the helper stream
-// concurrently with the tcgen05 kernel, and the merge waits for both.  `events` (optional)
+// Launches the decode kernels on `st`.  With `aux`, the tcgen05 and row kernels run on the
+// two helper streams concurrently, and the merge, on `st`, waits for both.  `events` (optional)
 // are recorded around each kernel on the stream it runs on.
 int launch_all(const fa::DecodeParams &p, const fa_plan *plan, cudaStream_t st, void **events, Aux *aux) {
     bool ev_ok = true;
@@ -170,20 +176,25 @@ int launch_all(const fa::DecodeParams &p, const fa_plan *plan, cudaStream_t st, 
     std::unique_lock<std::mutex> lk;
     if (both) {
         lk = std::unique_lock<std::mutex>(aux->mu);
-        if (cudaEventRecord(aux->fork, st) != cudaSuccess || cudaStreamWaitEvent(aux->stream, aux->fork, 0) != cudaSuccess)
+        if (cudaEventRecord(aux->fork, st) != cudaSuccess ||
+            cudaStreamWaitEvent(aux->tc_stream, aux->fork, 0) != cudaSuccess ||
+            cudaStreamWaitEvent(aux->row_stream, aux->fork, 0) != cudaSuccess)
             return FA_ERR_CUDA;
     }
-    cudaStream_t rs = both ? aux->stream : st;
-    rec(2, st);
+    cudaStream_t ts = both ? aux->tc_stream : st, rs = both ? aux->row_stream : st;
+    rec(2, ts);
     if (p.n_items_tc > 0)
-        fa::tck::tc_kernel<<<p.n_items_tc, fa::tck::kThreads, fa::tck::kSmemBytes, st>>>(p);
-    rec(3, st);
+        fa::tck::tc_kernel<<<p.n_items_tc, fa::tck::kThreads, fa::tck::kSmemBytes, ts>>>(p);
+    rec(3, ts);
     rec(0, rs);
     if (p.n_items > 0)
         fa::rowk::row_kernel<<<p.n_items, fa::rowk::kThreads, fa::rowk::kSmemBytes, rs>>>(p);
     rec(1, rs);
     if (both) {
-        if (cudaEventRecord(aux->join, aux->stream) != cudaSuccess || cudaStreamWaitEvent(st, aux->join, 0) != cudaSuccess)
+        if (cudaEventRecord(aux->join_tc, aux->tc_stream) != cudaSuccess ||
+            cudaEventRecord(aux->join_row, aux->row_stream) != cudaSuccess ||
+            cudaStreamWaitEvent(st, aux->join_tc, 0) != cudaSuccess ||
+            cudaStreamWaitEvent(st, aux->join_row, 0) != cudaSuccess)
             return FA_ERR_CUDA;
     }
     rec(4, st);
