@@ -184,6 +184,27 @@ def dist_setup(n_gpus):
     return None, 0, 1, 0
 
 
+def rank_workload(config, rank, device, values=True):
+    """Rank r's problem: the workload's structure with values drawn from seed + 1000 r (the
+    decode shards into independent problems, one per GPU: weak scaling, no collective on the
+    data path)."""
+    w = W.make(config, device=device, values=values and rank == 0)
+    if rank:
+        w.meta["seed"] += 1000 * rank
+        if values:
+            W.fill_values(w, device=device)
+    return w
+
+
+def max_over_ranks(dist, ms, device):
+    """The slowest rank's time per step (every rank gets it)."""
+    if dist is None:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def oracle_sample(w, budget_s, max_tasks=None):
     """Times the fp64 oracle on whole branches (all heads) until ~budget_s of CPU work."""
     import oracle
@@ -249,10 +270,7 @@ def run_ours(args):
     dist, rank, world, local = dist_setup(args.gpus)
     dev = torch.device("cuda", local if world > 1 else 0)
     torch.cuda.set_device(dev)
-    w = W.make(args.config, device=str(dev))
-    if rank:
-        w.meta["seed"] += 1000 * rank
-        W.fill_values(w, device=str(dev))  # an independent problem per rank (weak scaling)
+    w = rank_workload(args.config, rank, str(dev))
     t0 = time.perf_counter()
     run = fa.ForkAttention(w, out_dtype=fa.FA_BF16, device=dev)
     plan_s = time.perf_counter() - t0
@@ -294,11 +312,7 @@ def run_ours(args):
     step_ms = [a.elapsed_time(b) for a, b in zip(ev_start, ev_stop)]
     assert fa.fork_attn_check(run.plan, stream) == 0, "device error word set in the timed region"
     ms = sum(step_ms) / K
-    ms_max = ms
-    if dist:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_max = float(t.item())
+    ms_max = max_over_ranks(dist, ms, dev)
     value = unique_bytes * world / (ms_max * 1e-3) / 1e9
     bq_s = w.total_q * world / (ms_max * 1e-3)
 
