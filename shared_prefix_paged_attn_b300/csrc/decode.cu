@@ -84,7 +84,7 @@ int set_smem_attr() {
         cudaFuncAttributes fattr;
         if (cudaFuncGetAttributes(&fattr, fa::tck::tc_kernel) != cudaSuccess) return FA_ERR_CUDA;
         if (int64_t(fattr.numRegs) * fa::tck::kThreads <
-            128 * int64_t(fa::tck::kLowRegs) + 256 * int64_t(fa::tck::kHighRegs))
+            128 * int64_t(fa::tck::kLowRegs) + int64_t(fa::tck::kThreads - 128) * fa::tck::kHighRegs)
             return FA_ERR_UNSUPPORTED;
         done[dev] = true;
     }
