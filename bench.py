@@ -410,8 +410,8 @@ def run_ours(args):
             "per_kernel_pass": f"{Kk} steps, kernels run one after another (fork_attn_decode_timed)",
             "step_ms_min": min(step_ms), "step_ms_median": statistics.median(step_ms),
             "wall_s_timed_region": wall,
-            "gpu_launches": K * (int(st["num_items_rows"] > 0) + int(st["num_items_tensor"] > 0)
-                                 + int(st["merge_rows"] > 0)),
+            "gpu_launches": K * (int(st["num_items_row8"] > 0) + int(st["num_items_rows"] > st["num_items_row8"])
+                                 + int(st["num_items_tensor"] > 0) + int(st["merge_rows"] > 0)),
             "flops_per_step": st["flops_rows"] + st["flops_tensor"],
             "clocks": clk.record(),
             "e2e": e2e,

@@ -128,7 +128,7 @@ typedef struct {
     int64_t touched_pages;
     int64_t listed_visible_slots;  /* sum over branches of visible entries (copy-context)   */
     int64_t num_chunks;
-    int64_t num_items_rows;        /* work items of the CUDA-core/mma.sync row kernel       */
+    int64_t num_items_rows;        /* work items of the mma.sync row kernels                */
     int64_t num_items_tensor;      /* work items of the tcgen05 kernel                      */
     int64_t kv_bytes_rows;         /* K+V bytes read by the row kernel (all heads)           */
     int64_t kv_bytes_tensor;       /* K+V bytes read by the tcgen05 kernel                   */
@@ -139,7 +139,7 @@ typedef struct {
     int64_t unique_slots_tensor;   /* distinct visible physical slots read by tcgen05 kernel */
     int64_t flops_rows;            /* algorithmic flops of the row kernel: per visible slot  */
     int64_t flops_tensor;          /* of a reader, 4 x 128 x (query rows) per KV head        */
-    int64_t reserved[1];
+    int64_t num_items_row8;        /* of num_items_rows: items with <= 8 rows (own kernel)   */
 } fa_plan_stats;
 
 typedef struct fa_plan fa_plan; /* opaque; owned by the library */
@@ -184,7 +184,8 @@ int fork_attn_decode(const void *q, const void *k_pages, const void *v_pages,
 /* The same decode with its three kernels run one after the other on `stream` (no helper
  * stream), for timing each kernel alone: if `events` [host] is not NULL it is an array of
  * 2*n_events cudaEvent_t handles (as void*) recorded on `stream` around each kernel launch:
- * [start_0, stop_0, start_1, stop_1, start_2, stop_2] for the row kernel, the tcgen05 kernel
+ * [start_0, stop_0, start_1, stop_1, start_2, stop_2] for the row kernels (the one for
+ * <= 8 rows, then the one for up to 32), the tcgen05 kernel
  * and the merge kernel (an absent kernel records start = stop).  n_events must be 0 or 3.
  *
  * (fork_attn_decode itself, when a plan has work for both the row and the tcgen05 kernel,

@@ -44,7 +44,7 @@ class FaPlanStats(ctypes.Structure):
                 ("partial_rows", c_int64), ("merge_rows", c_int64), ("total_q", c_int64),
                 ("unique_slots_rows", c_int64), ("unique_slots_tensor", c_int64),
                 ("flops_rows", c_int64), ("flops_tensor", c_int64),
-                ("reserved", c_int64 * 1)]
+                ("num_items_row8", c_int64)]
 
 
 # name -> (restype, argtypes); every symbol declared in include/fork_attn.h

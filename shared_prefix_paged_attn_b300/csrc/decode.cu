@@ -7,6 +7,7 @@
 
 #include "merge_kernel.cuh"
 #include "plan_internal.h"
+#include "row8_kernel.cuh"
 #include "row_kernel.cuh"
 #include "tc_kernel.cuh"
 
@@ -77,7 +78,9 @@ int set_smem_attr() {
         if (cudaFuncSetAttribute(fa::rowk::row_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  int(fa::rowk::kSmemBytes)) != cudaSuccess ||
             cudaFuncSetAttribute(fa::tck::tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 int(fa::tck::kSmemBytes)) != cudaSuccess)
+                                 int(fa::tck::kSmemBytes)) != cudaSuccess ||
+            cudaFuncSetAttribute(fa::r8k::row8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(fa::r8k::kSmemBytes)) != cudaSuccess)
             return FA_ERR_CUDA;
         // the tcgen05 kernel re-splits its registers with setmaxnreg; the split must fit in
         // what the block is launched with, or the increase would wait forever
@@ -111,6 +114,7 @@ int fill_params(const fa_plan *plan, const void *q, const void *k_pages, const v
     p.chunks = reinterpret_cast<const fa::Chunk *>(base + L.chunks);
     p.items = reinterpret_cast<const fa::Item *>(base + L.items_rows);
     p.items_tc = reinterpret_cast<const fa::Item *>(base + L.items_tc);
+    p.items_r8 = reinterpret_cast<const fa::Item *>(base + L.items_r8);
     p.rows = reinterpret_cast<const fa::RowRec *>(base + L.rows);
     p.branches = reinterpret_cast<const fa::Branch *>(base + L.branches);
     p.q_merge = reinterpret_cast<const fa::QMerge *>(base + L.q_merge);
@@ -124,6 +128,7 @@ int fill_params(const fa_plan *plan, const void *q, const void *k_pages, const v
     p.scale_log2 = plan->dims.scale * 1.4426950408889634f;
     p.n_items = L.n_items_rows;
     p.n_items_tc = L.n_items_tc;
+    p.n_items_r8 = L.n_items_r8;
     p.pool_pages = int32_t(plan->num_pages_pool);
     p.total_rows = L.total_q * plan->dims.num_q_heads;
     return FA_OK;
@@ -139,7 +144,8 @@ bool needs_merge(const fa_plan *plan) { return plan->stats.merge_rows > 0; }
 struct Aux {
     cudaStream_t tc_stream = nullptr;   // highest priority: the tcgen05 kernel's CTAs go first
     cudaStream_t row_stream = nullptr;  // lowest priority: row CTAs fill the SMs left over
-    cudaEvent_t fork = nullptr, join_tc = nullptr, join_row = nullptr;
+    cudaStream_t row8_stream = nullptr;  // lowest priority, beside the other row kernel
+    cudaEvent_t fork = nullptr, join_tc = nullptr, join_row = nullptr, join_row8 = nullptr;
     std::mutex mu;  // the events are shared by every decode on the device
 };
 
@@ -155,6 +161,8 @@ Aux *aux_for_current_device() {
         if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess ||
             cudaStreamCreateWithPriority(&aux[dev].tc_stream, cudaStreamNonBlocking, greatest) != cudaSuccess ||
             cudaStreamCreateWithPriority(&aux[dev].row_stream, cudaStreamNonBlocking, least) != cudaSuccess ||
+            cudaStreamCreateWithPriority(&aux[dev].row8_stream, cudaStreamNonBlocking, least) != cudaSuccess ||
+            cudaEventCreateWithFlags(&aux[dev].join_row8, cudaEventDisableTiming) != cudaSuccess ||
             cudaEventCreateWithFlags(&aux[dev].fork, cudaEventDisableTiming) != cudaSuccess ||
             cudaEventCreateWithFlags(&aux[dev].join_tc, cudaEventDisableTiming) != cudaSuccess ||
             cudaEventCreateWithFlags(&aux[dev].join_row, cudaEventDisableTiming) != cudaSuccess)
@@ -172,29 +180,37 @@ int launch_all(const fa::DecodeParams &p, const fa_plan *plan, cudaStream_t st, 
     auto rec = [&](int i, cudaStream_t s) {
         if (events) ev_ok = ev_ok && cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s) == cudaSuccess;
     };
-    const bool both = aux && p.n_items > 0 && p.n_items_tc > 0;
+    const int kinds = int(p.n_items > 0) + int(p.n_items_r8 > 0) + int(p.n_items_tc > 0);
+    const bool both = aux && kinds > 1;
     std::unique_lock<std::mutex> lk;
     if (both) {
         lk = std::unique_lock<std::mutex>(aux->mu);
         if (cudaEventRecord(aux->fork, st) != cudaSuccess ||
             cudaStreamWaitEvent(aux->tc_stream, aux->fork, 0) != cudaSuccess ||
-            cudaStreamWaitEvent(aux->row_stream, aux->fork, 0) != cudaSuccess)
+            cudaStreamWaitEvent(aux->row_stream, aux->fork, 0) != cudaSuccess ||
+            cudaStreamWaitEvent(aux->row8_stream, aux->fork, 0) != cudaSuccess)
             return FA_ERR_CUDA;
     }
     cudaStream_t ts = both ? aux->tc_stream : st, rs = both ? aux->row_stream : st;
+    cudaStream_t r8s = both ? aux->row8_stream : st;
     rec(2, ts);
     if (p.n_items_tc > 0)
         fa::tck::tc_kernel<<<p.n_items_tc, fa::tck::kThreads, fa::tck::kSmemBytes, ts>>>(p);
     rec(3, ts);
+    // the per-kernel events (sequential decode only) span both row kernels
     rec(0, rs);
+    if (p.n_items_r8 > 0)
+        fa::r8k::row8_kernel<<<p.n_items_r8, fa::r8k::kThreads, fa::r8k::kSmemBytes, r8s>>>(p);
     if (p.n_items > 0)
         fa::rowk::row_kernel<<<p.n_items, fa::rowk::kThreads, fa::rowk::kSmemBytes, rs>>>(p);
     rec(1, rs);
     if (both) {
         if (cudaEventRecord(aux->join_tc, aux->tc_stream) != cudaSuccess ||
             cudaEventRecord(aux->join_row, aux->row_stream) != cudaSuccess ||
+            cudaEventRecord(aux->join_row8, aux->row8_stream) != cudaSuccess ||
             cudaStreamWaitEvent(st, aux->join_tc, 0) != cudaSuccess ||
-            cudaStreamWaitEvent(st, aux->join_row, 0) != cudaSuccess)
+            cudaStreamWaitEvent(st, aux->join_row, 0) != cudaSuccess ||
+            cudaStreamWaitEvent(st, aux->join_row8, 0) != cudaSuccess)
             return FA_ERR_CUDA;
     }
     rec(4, st);
@@ -339,6 +355,7 @@ extern "C" int fork_attn_decode_static_scratch(const void *q, const void *k_page
     p.chunks = reinterpret_cast<const fa::Chunk *>(base + L.chunks);
     p.items = reinterpret_cast<const fa::Item *>(base + L.items_rows);
     p.items_tc = reinterpret_cast<const fa::Item *>(base + L.items_tc);
+    p.items_r8 = reinterpret_cast<const fa::Item *>(base + L.items_r8);
     p.rows = reinterpret_cast<const fa::RowRec *>(base + L.rows);
     p.branches = reinterpret_cast<const fa::Branch *>(base + L.branches);
     p.q_merge = reinterpret_cast<const fa::QMerge *>(base + L.q_merge);

@@ -21,6 +21,7 @@ struct DecodeParams {
     const Chunk *chunks;
     const Item *items;     // row-kernel work items
     const Item *items_tc;  // tcgen05-kernel work items
+    const Item *items_r8;  // work items of the row kernel for <= 8 rows
     const RowRec *rows;
     const Branch *branches;
     const QMerge *q_merge;
@@ -31,6 +32,7 @@ struct DecodeParams {
     float scale_log2;  // scale * log2(e): scores are kept in base 2 inside the kernels
     int32_t n_items;
     int32_t n_items_tc;
+    int32_t n_items_r8;
     int32_t pool_pages;  // page index one past the pool: TMA reads it as zeros
     int32_t total_rows;  // total_q * Hq
 };

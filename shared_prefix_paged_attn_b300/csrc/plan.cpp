@@ -258,7 +258,7 @@ struct Emit {
     std::vector<int32_t> chunk_pages;
     std::vector<fa::Chunk> chunks;
     std::vector<fa::Occ> occs;
-    std::vector<fa::Item> items_rows, items_tc;
+    std::vector<fa::Item> items_rows, items_tc, items_r8;
     std::vector<fa::RowRec> rows;
     std::vector<fa::Branch> branches;
     std::vector<fa::QMerge> q_merge;
@@ -427,7 +427,7 @@ int build_plan(Input &in, const fa_plan_opts &opts, fa_plan *plan) {
                     em.items_tc.push_back(it);
                     st.kv_bytes_tensor += kv;
                 } else {
-                    em.items_rows.push_back(it);
+                    (it.n_rows <= 8 ? em.items_r8 : em.items_rows).push_back(it);
                     st.kv_bytes_rows += kv;
                 }
             }
@@ -442,13 +442,16 @@ int build_plan(Input &in, const fa_plan_opts &opts, fa_plan *plan) {
     };
     std::stable_sort(em.items_tc.begin(), em.items_tc.end(), by_len);
     std::stable_sort(em.items_rows.begin(), em.items_rows.end(), by_len);
+    std::stable_sort(em.items_r8.begin(), em.items_r8.end(), by_len);
 
     st.num_chunks = int64_t(em.chunks.size());
-    st.num_items_rows = int64_t(em.items_rows.size());
+    st.num_items_rows = int64_t(em.items_rows.size()) + int64_t(em.items_r8.size());
+    st.num_items_row8 = int64_t(em.items_r8.size());
     st.num_items_tensor = int64_t(em.items_tc.size());
     st.partial_rows = prow;
     st.total_q = in.q_off[B];
     if (em.items_rows.size() > size_t(INT32_MAX) || em.items_tc.size() > size_t(INT32_MAX) ||
+        em.items_r8.size() > size_t(INT32_MAX) ||
         em.chunk_pages.size() > size_t(INT32_MAX))
         return FA_ERR_UNSUPPORTED;
 
@@ -461,6 +464,7 @@ int build_plan(Input &in, const fa_plan_opts &opts, fa_plan *plan) {
     L.chunks = place(int64_t(em.chunks.size()) * sizeof(fa::Chunk));
     L.items_rows = place(int64_t(em.items_rows.size()) * sizeof(fa::Item));
     L.items_tc = place(int64_t(em.items_tc.size()) * sizeof(fa::Item));
+    L.items_r8 = place(int64_t(em.items_r8.size()) * sizeof(fa::Item));
     L.rows = place(int64_t(em.rows.size()) * sizeof(fa::RowRec));
     L.branches = place(int64_t(em.branches.size()) * sizeof(fa::Branch));
     L.q_merge = place(int64_t(em.q_merge.size()) * sizeof(fa::QMerge));
@@ -471,6 +475,7 @@ int build_plan(Input &in, const fa_plan_opts &opts, fa_plan *plan) {
     L.n_chunks = int32_t(em.chunks.size());
     L.n_items_rows = int32_t(em.items_rows.size());
     L.n_items_tc = int32_t(em.items_tc.size());
+    L.n_items_r8 = int32_t(em.items_r8.size());
     L.n_rows = int32_t(em.rows.size());
     L.n_branches = B;
     L.total_q = in.q_off[B];
@@ -482,6 +487,7 @@ int build_plan(Input &in, const fa_plan_opts &opts, fa_plan *plan) {
     put(L.chunks, em.chunks.data(), em.chunks.size() * sizeof(fa::Chunk));
     put(L.items_rows, em.items_rows.data(), em.items_rows.size() * sizeof(fa::Item));
     put(L.items_tc, em.items_tc.data(), em.items_tc.size() * sizeof(fa::Item));
+    put(L.items_r8, em.items_r8.data(), em.items_r8.size() * sizeof(fa::Item));
     put(L.rows, em.rows.data(), em.rows.size() * sizeof(fa::RowRec));
     put(L.branches, em.branches.data(), em.branches.size() * sizeof(fa::Branch));
     put(L.q_merge, em.q_merge.data(), em.q_merge.size() * sizeof(fa::QMerge));

@@ -82,9 +82,9 @@ struct QMerge {
 // Byte offsets of the arrays inside the device plan buffer.  The first 256 bytes hold the
 // device error word (int32 at offset 0).
 struct Layout {
-    int64_t chunk_pages, chunks, items_rows, items_tc, rows, branches, q_merge, merge_bases,
+    int64_t chunk_pages, chunks, items_rows, items_tc, items_r8, rows, branches, q_merge, merge_bases,
         mask_words, total;
-    int32_t n_chunk_pages, n_chunks, n_items_rows, n_items_tc, n_rows, n_branches, total_q,
+    int32_t n_chunk_pages, n_chunks, n_items_rows, n_items_tc, n_items_r8, n_rows, n_branches, total_q,
         n_merge_bases, n_mask_words;
 };
 

@@ -111,6 +111,14 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// Transpose of an 8x8 matrix of 16-bit elements held as a warp fragment (lane gid*4 + tig holds
+// row gid, columns 2 tig and 2 tig + 1): returns the fragment of the transposed matrix.
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
 // 2^x with the hardware approximation (flushes subnormals; ex2(-inf) = 0).
 __device__ __forceinline__ float ex2(float x) {
     float y;
