@@ -48,33 +48,29 @@ __global__ void __launch_bounds__(kThreads) merge_kernel(const __grid_constant__
                 pr = bases[k0 + lane] + off;
                 wl = expf(p.part_lse[pr] - M);
             }
-            // the O terms in the plan's order, eight loads in flight
-            int k = 0;
-            for (; k + 8 <= kn; k += 8) {
+            // the O terms in the plan's order, eight loads in flight (the last group is
+            // predicated rather than walked one partial at a time)
+            for (int k = 0; k < kn; k += 8) {
                 float w[8];
                 int r[8];
                 float4 v[8];
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
-                    w[u] = __shfl_sync(0xffffffffu, wl, k + u);
-                    r[u] = __shfl_sync(0xffffffffu, pr, k + u);
+                    w[u] = __shfl_sync(0xffffffffu, wl, (k + u) & 31);
+                    r[u] = __shfl_sync(0xffffffffu, pr, (k + u) & 31);
                 }
 #pragma unroll
                 for (int u = 0; u < 8; ++u)
-                    v[u] = *reinterpret_cast<const float4 *>(p.part_o + size_t(r[u]) * kHeadDim + lane * 4);
+                    v[u] = k + u < kn ? *reinterpret_cast<const float4 *>(p.part_o + size_t(r[u]) * kHeadDim + lane * 4)
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
-                    L += w[u];
-                    acc.x += w[u] * v[u].x; acc.y += w[u] * v[u].y;
-                    acc.z += w[u] * v[u].z; acc.w += w[u] * v[u].w;
+                    if (k + u < kn) {
+                        L += w[u];
+                        acc.x += w[u] * v[u].x; acc.y += w[u] * v[u].y;
+                        acc.z += w[u] * v[u].z; acc.w += w[u] * v[u].w;
+                    }
                 }
-            }
-            for (; k < kn; ++k) {
-                const float w = __shfl_sync(0xffffffffu, wl, k);
-                const int r = __shfl_sync(0xffffffffu, pr, k);
-                const float4 v = *reinterpret_cast<const float4 *>(p.part_o + size_t(r) * kHeadDim + lane * 4);
-                L += w;
-                acc.x += w * v.x; acc.y += w * v.y; acc.z += w * v.z; acc.w += w * v.w;
             }
         }
         const float inv = 1.f / L;
