@@ -301,14 +301,15 @@ __device__ __forceinline__ void softmax(const DecodeParams &p, Smem &sm, const C
             for (int c = 0; c < 128; ++c)
                 if (!((bits[c >> 5] >> (c & 31)) & 1u)) s[c] = __float_as_uint(-INFINITY);
         }
-        // row max with eight independent chains (short dependency latency)
+        // row max with eight independent chains of three-input maxima
         float mxk[8];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) mxk[k] = __uint_as_float(s[k]);
+        for (int k = 0; k < 8; ++k) mxk[k] = fmaxf(__uint_as_float(s[k]), __uint_as_float(s[k + 8]));
 #pragma unroll
-        for (int c = 8; c < 128; c += 8)
+        for (int c = 16; c < 128; c += 16)
 #pragma unroll
-            for (int k = 0; k < 8; ++k) mxk[k] = fmaxf(mxk[k], __uint_as_float(s[c + k]));
+            for (int k = 0; k < 8; ++k)
+                mxk[k] = ptx::fmax3(mxk[k], __uint_as_float(s[c + k]), __uint_as_float(s[c + k + 8]));
         float mx = fmaxf(fmaxf(fmaxf(mxk[0], mxk[1]), fmaxf(mxk[2], mxk[3])),
                          fmaxf(fmaxf(mxk[4], mxk[5]), fmaxf(mxk[6], mxk[7])));
         if (!valid) mx = 0.f;  // a padding row (zero Q) in a warp with real rows: finite junk
@@ -325,22 +326,35 @@ __device__ __forceinline__ void softmax(const DecodeParams &p, Smem &sm, const C
         }
         const float muse = mrun == -INFINITY ? 0.f : mrun;
 
-        // P = 2^(s * scale * log2 e - m) as bf16 pairs over the first 64 columns of S
-        float rsk[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        // P = 2^(s * scale * log2 e - m) as bf16 pairs over the first 64 columns of S; the
+        // scale-and-subtract and the row sum run on packed fp32 pairs
+        const uint64_t sc2 = ptx::f2(sl2, sl2), nm2 = ptx::f2(-muse, -muse);
+        uint64_t rs2[4] = {0ull, 0ull, 0ull, 0ull};  // four pair-chains of the row sum
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
             uint32_t pk[16];
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
-                const float x = ptx::ex2(fmaf(__uint_as_float(s[32 * h + 2 * c]), sl2, -muse));
-                const float y = ptx::ex2(fmaf(__uint_as_float(s[32 * h + 2 * c + 1]), sl2, -muse));
-                rsk[c & 7] += x + y;
+                float x, y;
+                ptx::f2_split(ptx::ffma2(ptx::f2(__uint_as_float(s[32 * h + 2 * c]), __uint_as_float(s[32 * h + 2 * c + 1])),
+                                         sc2, nm2),
+                              x, y);
+                x = ptx::ex2(x);
+                y = ptx::ex2(y);
+                rs2[c & 3] = ptx::fadd2(rs2[c & 3], ptx::f2(x, y));
                 pk[c] = ptx::pack_bf16(x, y);
             }
             // columns 16h .. 16h+15 held scores already in registers
             tc::st16(tS + 16 * h, pk);
         }
-        lrun += ((rsk[0] + rsk[1]) + (rsk[2] + rsk[3])) + ((rsk[4] + rsk[5]) + (rsk[6] + rsk[7]));
+        {
+            float a0, a1, b0, b1, c0, c1, d0, d1;
+            ptx::f2_split(rs2[0], a0, a1);
+            ptx::f2_split(rs2[1], b0, b1);
+            ptx::f2_split(rs2[2], c0, c1);
+            ptx::f2_split(rs2[3], d0, d1);
+            lrun += ((a0 + a1) + (b0 + b1)) + ((c0 + c1) + (d0 + d1));
+        }
 
         if (rescale) {
             // O of the previous tiles (the P V MMA of tile j-1 must be done) times alpha
