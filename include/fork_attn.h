@@ -116,7 +116,8 @@ typedef struct {
     int32_t num_sms;        /* SMs to plan for (0 = 148)                                     */
     int32_t tensor_min_rows;/* reader-set rows at which a run goes to the tcgen05 kernel    */
                             /* (0 = default; < 0 = never)                                    */
-    int32_t reserved[5];
+    int32_t reserved[5];    /* [0] > 0: persistent CTAs of the tcgen05 kernel (0 = from the  */
+                            /* planner's split of SMs between it and the row kernels)        */
 } fa_plan_opts;
 
 /* Counters of a plan, for measurement.  unique_visible_slots: distinct physical token slots

@@ -130,6 +130,7 @@ int fill_params(const fa_plan *plan, const void *q, const void *k_pages, const v
     p.n_items_tc = L.n_items_tc;
     p.n_items_r8 = L.n_items_r8;
     p.pool_pages = int32_t(plan->num_pages_pool);
+    p.tc_ctas = plan->tc_ctas;
     p.total_rows = L.total_q * plan->dims.num_q_heads;
     return FA_OK;
 }
@@ -195,7 +196,7 @@ int launch_all(const fa::DecodeParams &p, const fa_plan *plan, cudaStream_t st, 
     cudaStream_t r8s = both ? aux->row8_stream : st;
     rec(2, ts);
     if (p.n_items_tc > 0)
-        fa::tck::tc_kernel<<<p.n_items_tc, fa::tck::kThreads, fa::tck::kSmemBytes, ts>>>(p);
+        fa::tck::tc_kernel<<<p.tc_ctas, fa::tck::kThreads, fa::tck::kSmemBytes, ts>>>(p);
     rec(3, ts);
     // the per-kernel events (sequential decode only) span both row kernels
     rec(0, rs);

@@ -33,6 +33,7 @@ struct DecodeParams {
     int32_t n_items;
     int32_t n_items_tc;
     int32_t n_items_r8;
+    int32_t tc_ctas;  // persistent CTAs of the tcgen05 kernel
     int32_t pool_pages;  // page index one past the pool: TMA reads it as zeros
     int32_t total_rows;  // total_q * Hq
 };

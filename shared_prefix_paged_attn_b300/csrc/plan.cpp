@@ -444,6 +444,25 @@ int build_plan(Input &in, const fa_plan_opts &opts, fa_plan *plan) {
     std::stable_sort(em.items_rows.begin(), em.items_rows.end(), by_len);
     std::stable_sort(em.items_r8.begin(), em.items_r8.end(), by_len);
 
+    // Persistent CTAs of the tcgen05 kernel: the SMs it holds while the row kernels stream
+    // the private runs on the others.  Its work is compute (about 1.14 us of one SM per
+    // 128-token tile of one 128-row M tile), theirs is memory (about 130 GB/s per SM they
+    // hold); the split gives each side SMs in proportion to its SM time.  (Both constants are
+    // fitted to B300 sweeps of the split; fa_plan_opts.reserved[0] > 0 overrides the count.)
+    {
+        double w_tc = 0.0;
+        for (const fa::Item &it : em.items_tc) {
+            const int T = (em.chunks[it.chunk].n_pages + 7) / 8;
+            w_tc += T * (it.n_rows > fa::kTcRows ? 2.0 : 1.0) * 1.14e-6;
+        }
+        const double w_row = double(st.kv_bytes_rows) / 130e9;
+        const int sms = opts.num_sms > 0 ? opts.num_sms : 148;
+        int n = w_tc + w_row > 0.0 ? int(std::lround(sms * w_tc / (w_tc + w_row))) : sms;
+        if (opts.reserved[0] > 0) n = opts.reserved[0];
+        n = std::max(1, std::min(n, sms));
+        plan->tc_ctas = int32_t(std::min<int64_t>(n, std::max<size_t>(em.items_tc.size(), 1)));
+    }
+
     st.num_chunks = int64_t(em.chunks.size());
     st.num_items_rows = int64_t(em.items_rows.size()) + int64_t(em.items_r8.size());
     st.num_items_row8 = int64_t(em.items_r8.size());

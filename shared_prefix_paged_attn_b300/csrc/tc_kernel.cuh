@@ -62,6 +62,7 @@ struct Smem {
     uint64_t sfull[2], pfull[2], odone[2], fin;
     uint32_t tmem_base;
     int32_t abort;
+    int32_t item;  // the work item the CTA is on (persistent CTAs take items from a queue)
 };
 constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
 static_assert(kSmemBytes <= 232448, "fits the 227 KiB opt-in shared memory of one CTA");
@@ -233,11 +234,22 @@ __device__ __forceinline__ void mma_issuer(Smem &sm, uint32_t tmem, int T, int m
     }
     if (ok) pv(T - 1);
     if (!ok && lane == 0) *reinterpret_cast<volatile int32_t *>(&sm.abort) = 1;
-    // all MMAs issued by either MMA warp are complete before TMEM is freed (fin takes one
-    // arrival per M tile)
+    // all MMAs issued by either MMA warp are complete before TMEM is reused or freed (fin
+    // takes one arrival per M tile), and the last arrivals on the stage-free barriers have
+    // landed before the barriers are re-initialised for the next item
     commit(sm.fin);
     const volatile int32_t never = 0;
     wait_bar(ptx::smem_u32(&sm.fin), 0, &never);
+    if (ok) {
+        for (int st = 0; st < kKStages && st < T; ++st) {
+            const int jl = st + ((T - 1 - st) / kKStages) * kKStages;  // last tile on stage st
+            wait_bar(ptx::smem_u32(&sm.kfree[st]), (jl / kKStages) & 1, &never);
+        }
+        for (int st = 0; st < kVStages && st < T; ++st) {
+            const int jl = st + ((T - 1 - st) / kVStages) * kVStages;
+            wait_bar(ptx::smem_u32(&sm.vfree[st]), (jl / kVStages) & 1, &never);
+        }
+    }
 }
 
 __device__ __forceinline__ void softmax(const DecodeParams &p, Smem &sm, const Chunk &ch, const Row &ri, bool valid, uint32_t tmem,
@@ -428,89 +440,152 @@ __device__ __forceinline__ void softmax(const DecodeParams &p, Smem &sm, const C
     }
 }
 
+__device__ __forceinline__ void init_barriers(Smem &sm, int MT) {
+    for (int s = 0; s < kKStages; ++s) {
+        ptx::mbar_init(ptx::smem_u32(&sm.kfull[s]), 1);
+        ptx::mbar_init(ptx::smem_u32(&sm.kfree[s]), MT);  // one arrival per MMA warp
+    }
+    for (int s = 0; s < kVStages; ++s) {
+        ptx::mbar_init(ptx::smem_u32(&sm.vfull[s]), 1);
+        ptx::mbar_init(ptx::smem_u32(&sm.vfree[s]), MT);
+    }
+    for (int m = 0; m < 2; ++m) {
+        ptx::mbar_init(ptx::smem_u32(&sm.sfull[m]), 1);
+        ptx::mbar_init(ptx::smem_u32(&sm.pfull[m]), 128);
+        ptx::mbar_init(ptx::smem_u32(&sm.odone[m]), 1);
+    }
+    ptx::mbar_init(ptx::smem_u32(&sm.fin), MT);
+    ptx::fence_mbar_init();
+}
+
+__device__ __forceinline__ void inval_barriers(Smem &sm) {
+    uint64_t *first = &sm.kfull[0], *last = &sm.fin;
+    for (uint64_t *b = first; b <= last; ++b) ptx::mbar_inval(ptx::smem_u32(b));
+}
+
+// Persistent: p.tc_ctas CTAs (one per SM) take work items from a counter in the plan buffer
+// (header word 1) until none is left, so that the SMs they leave to the row kernels are
+// known and a CTA that runs out of work frees its SM at once.  The last CTA to leave resets
+// the counters (header words 1 and 2) for the next decode.
 __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__ DecodeParams p) {
     extern __shared__ uint8_t smem_raw[];
     Smem &sm = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const Item it = p.items_tc[blockIdx.x];
-    const Chunk ch = p.chunks[it.chunk];
-    const int T = (ch.n_pages + kTilePages - 1) / kTilePages;
-    const int MT = it.n_rows > kTcRows ? 2 : 1;
-    if (ch.n_pages > kMaxChunkPages || it.n_rows > kRows) {  // never planned; refuse, uniformly
-        if (threadIdx.x == 0) atomicOr(p.err, kErrBounds);
-        return;
-    }
+    int32_t *queue = p.err + 1, *done = p.err + 2;
+
+    auto item_ok = [&](int i) {  // items the planner never makes are refused, uniformly
+        const Item it = p.items_tc[i];
+        return p.chunks[it.chunk].n_pages <= kMaxChunkPages && it.n_rows <= kRows;
+    };
+    // the next item this CTA runs (a refused item sets the error word and is skipped)
+    auto next_item = [&]() {
+        int i = atomicAdd(queue, 1);
+        while (i < p.n_items_tc && !item_ok(i)) {
+            atomicOr(p.err, kErrBounds);
+            i = atomicAdd(queue, 1);
+        }
+        return i;
+    };
+    auto item_mt = [&](int i) { return p.items_tc[i].n_rows > kTcRows ? 2 : 1; };
 
     if (tid == 0) {
-        for (int s = 0; s < kKStages; ++s) {
-            ptx::mbar_init(ptx::smem_u32(&sm.kfull[s]), 1);
-            ptx::mbar_init(ptx::smem_u32(&sm.kfree[s]), MT);  // one arrival per MMA warp
-        }
-        for (int s = 0; s < kVStages; ++s) {
-            ptx::mbar_init(ptx::smem_u32(&sm.vfull[s]), 1);
-            ptx::mbar_init(ptx::smem_u32(&sm.vfree[s]), MT);
-        }
-        for (int m = 0; m < 2; ++m) {
-            ptx::mbar_init(ptx::smem_u32(&sm.sfull[m]), 1);
-            ptx::mbar_init(ptx::smem_u32(&sm.pfull[m]), 128);
-            ptx::mbar_init(ptx::smem_u32(&sm.odone[m]), 1);
-        }
-        ptx::mbar_init(ptx::smem_u32(&sm.fin), MT);
         sm.abort = 0;
-        ptx::fence_mbar_init();
+        sm.item = next_item();
+        if (sm.item < p.n_items_tc) init_barriers(sm, item_mt(sm.item));
     }
     if (warp == 1) {
         tc::tmem_alloc(ptx::smem_u32(&sm.tmem_base), kTmemCols);
         tc::tmem_relinquish();
     }
-    // softmax threads: their row's table entry, and the stacked Q row -> shared memory,
-    // 128-byte swizzled K-major (zeros for padding rows)
-    Row ri{0, 0x3fffffff, -1, -1};
-    bool valid = false;
-    const int sm_m = (warp >> 2) - 1;  // softmax warpgroup = M tile (warps 4-7, 8-11)
-    if (warp >= 4) {
-        // TMEM lane quarter of a warp is warp % 4, so row = 128 m + 32 (warp % 4) + lane
-        const int r = sm_m * kTcRows + (warp & 3) * 32 + lane;
-        valid = r < it.n_rows;
-        if (valid) ri = item_row(p, it, r);
-#pragma unroll 4
-        for (int c = 0; c < 16; ++c) {
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (valid) v = __ldg(reinterpret_cast<const uint4 *>(p.q + size_t(ri.qrow) * kHeadDim + c * 8));
-            *reinterpret_cast<uint4 *>(sm.q + (c >> 3) * kQHalf + r * 128 + (((c & 7) ^ (r & 7)) << 4)) = v;
-        }
-    }
-    tc::fence_proxy_async_smem();
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
     const uint32_t tmem = sm.tmem_base;
 
     // Each role ends the kernel in its own branch: code after a register re-split must not
-    // be shared by warps with different register counts.
+    // be shared by warps with different register counts.  Both branches run the same
+    // sequence of CTA barriers: per item B (barriers, Q ready), C (item done), D (next item
+    // known); then E before TMEM is freed.
     if (warp < 4) {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kLowRegs));
-        if (warp == 0) {
-            producer<false>(p, sm, it, ch, T, lane);
-        } else if (warp == 1) {
-            mma_issuer(sm, tmem, T, 0, lane);
-        } else if (warp == 3) {
-            if (MT > 1) mma_issuer(sm, tmem, T, 1, lane);
-        } else if (warp == 2) {
-            producer<true>(p, sm, it, ch, T, lane);
+        for (;;) {
+            const int i = sm.item;
+            if (i >= p.n_items_tc) break;
+            const Item it = p.items_tc[i];
+            const Chunk ch = p.chunks[it.chunk];
+            const int T = (ch.n_pages + kTilePages - 1) / kTilePages;
+            const int MT = it.n_rows > kTcRows ? 2 : 1;
+            tc::fence_before();
+            __syncthreads();  // B
+            tc::fence_after();
+            if (warp == 0) {
+                producer<false>(p, sm, it, ch, T, lane);
+            } else if (warp == 1) {
+                mma_issuer(sm, tmem, T, 0, lane);
+            } else if (warp == 3) {
+                if (MT > 1) mma_issuer(sm, tmem, T, 1, lane);
+            } else if (warp == 2) {
+                producer<true>(p, sm, it, ch, T, lane);
+            }
+            tc::fence_before();
+            __syncthreads();  // C
+            tc::fence_after();
+            if (tid == 0) {
+                inval_barriers(sm);
+                sm.item = sm.abort ? p.n_items_tc : next_item();
+                if (sm.item < p.n_items_tc) init_barriers(sm, item_mt(sm.item));
+            }
+            __syncthreads();  // D
+        }
+        if (tid == 0) {
+            if (sm.abort) atomicOr(p.err, kErrTimeout);
+            __threadfence();
+            if (atomicAdd(done, 1) == int(gridDim.x) - 1) {  // no CTA reads the queue any more
+                atomicExch(queue, 0);
+                atomicExch(done, 0);
+            }
         }
         tc::fence_before();
-        __syncthreads();
+        __syncthreads();  // E
         if (warp == 1) {
             tc::fence_after();
             tc::tmem_dealloc(tmem, kTmemCols);
         }
-        if (tid == 0 && sm.abort) atomicOr(p.err, kErrTimeout);
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kHighRegs));
-        if (sm_m < MT) softmax(p, sm, ch, ri, valid, tmem, T, sm_m, warp & 3, lane);
+        const int sm_m = (warp >> 2) - 1;  // softmax warpgroup = M tile (warps 4-7, 8-11)
+        // TMEM lane quarter of a warp is warp % 4, so row = 128 m + 32 (warp % 4) + lane
+        const int r = sm_m * kTcRows + (warp & 3) * 32 + lane;
+        for (;;) {
+            const int i = sm.item;
+            if (i >= p.n_items_tc) break;
+            const Item it = p.items_tc[i];
+            const Chunk ch = p.chunks[it.chunk];
+            const int T = (ch.n_pages + kTilePages - 1) / kTilePages;
+            const int MT = it.n_rows > kTcRows ? 2 : 1;
+            // the row's table entry, and its Q row -> shared memory, 128-byte swizzled K-major
+            // (zeros for padding rows); the previous item's MMAs are all done (barrier C)
+            Row ri{0, 0x3fffffff, -1, -1};
+            const bool valid = r < it.n_rows;
+            if (valid) ri = item_row(p, it, r);
+#pragma unroll 4
+            for (int c = 0; c < 16; ++c) {
+                uint4 v = make_uint4(0, 0, 0, 0);
+                if (valid) v = __ldg(reinterpret_cast<const uint4 *>(p.q + size_t(ri.qrow) * kHeadDim + c * 8));
+                *reinterpret_cast<uint4 *>(sm.q + (c >> 3) * kQHalf + r * 128 + (((c & 7) ^ (r & 7)) << 4)) = v;
+            }
+            tc::fence_proxy_async_smem();
+            tc::fence_before();
+            __syncthreads();  // B
+            tc::fence_after();
+            if (sm_m < MT) softmax(p, sm, ch, ri, valid, tmem, T, sm_m, warp & 3, lane);
+            tc::fence_before();
+            __syncthreads();  // C
+            tc::fence_after();
+            __syncthreads();  // D
+        }
         tc::fence_before();
-        __syncthreads();
+        __syncthreads();  // E
     }
 }
 
