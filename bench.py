@@ -280,11 +280,12 @@ def run_ours(args):
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     q, k, v = w.q, w.k_pages, w.v_pages
 
-    def step(events=None):
+    def step(events=None, concurrent=True):
         if events is None:
             fa.fork_attn_decode(q, k, v, run.plan, run.out, run.lse, stream)
         else:
-            fa.fork_attn_decode_timed(q, k, v, run.plan, run.out, run.lse, events, stream)
+            fa.fork_attn_decode_timed(q, k, v, run.plan, run.out, run.lse, events, stream,
+                                      concurrent=concurrent)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -292,9 +293,14 @@ def run_ours(args):
     torch.cuda.synchronize(dev)
     assert fa.fork_attn_check(run.plan, stream) == 0, "device error word set during warm-up"
 
+    # The timed region: each step is the decode as fork_attn_decode runs it (its kernels
+    # concurrent on helper streams), with CUDA events recorded around every kernel on the
+    # stream that kernel runs on, so that per-kernel durations come from the timed steps.
     K = args.steps
+    names = ["row8_kernel", "row_kernel", "tcgen05_kernel", "merge_kernel"]
     ev_start = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     ev_stop = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * len(names))] for _ in range(K)]
     if dist:
         dist.barrier()
     torch.cuda.synchronize(dev)
@@ -303,7 +309,7 @@ def run_ours(args):
         for i in range(K):
             flush.zero_()
             ev_start[i].record(stream)
-            step()
+            step(kev[i])
             ev_stop[i].record(stream)
         torch.cuda.synchronize(dev)
     wall = time.perf_counter() - wall0
@@ -315,41 +321,42 @@ def run_ours(args):
     ms_max = max_over_ranks(dist, ms, dev)
     value = unique_bytes * world / (ms_max * 1e-3) / 1e9
     bq_s = w.total_q * world / (ms_max * 1e-3)
+    avg = [sum(kev[i][2 * j].elapsed_time(kev[i][2 * j + 1]) for i in range(K)) / K
+           for j in range(len(names))]
 
-    # Per-kernel durations: the decode's kernels overlap in the timed region (the row kernel
-    # runs on a helper stream beside the tcgen05 kernel), so each kernel is timed alone in a
-    # second pass of the same decode with its kernels run one after another
-    # (fork_attn_decode_timed), L2 flushed before every step as above.
-    Kk = min(K, 200)
-    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(Kk)]
-    for i in range(Kk):
+    # For comparison, each kernel alone: the same decode with its kernels one after another
+    # on `stream` (L2 flushed before every step as above).
+    Ka = min(K, 50)
+    aev = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * len(names))] for _ in range(Ka)]
+    for i in range(Ka):
         flush.zero_()
-        step(kev[i])
+        step(aev[i], concurrent=False)
     torch.cuda.synchronize(dev)
     assert fa.fork_attn_check(run.plan, stream) == 0, "device error word set in the per-kernel pass"
-    kern_ms = [[kev[i][2 * j].elapsed_time(kev[i][2 * j + 1]) for i in range(Kk)] for j in range(3)]
-    names = ["row_kernel", "tcgen05_kernel", "merge_kernel"]
-    avg = [sum(x) / Kk for x in kern_ms]
+    alone = [sum(aev[i][2 * j].elapsed_time(aev[i][2 * j + 1]) for i in range(Ka)) / Ka
+             for j in range(len(names))]
+
     hbm_peak, peak_kind = peaks()
     tflops_peak, tpeak_kind = tensor_peak()
     traffic = ncu_traffic(w.name)
     part_bytes = st["partial_rows"] * (128 * 4 + 4) * 2  # fp32 partial O + lse, written then read
+    slots = {"row8_kernel": st["unique_slots_row8"], "row_kernel": st["unique_slots_row32"]}
     kernels = {}
     for j, n in enumerate(names):
         if avg[j] <= 0:
             continue
         if n == "tcgen05_kernel":
-            ach = st["flops_tensor"] / (avg[j] * 1e-3) / 1e12
-            kernels[n] = {"bound": "tensor", "achieved": ach, "peak": tflops_peak, "unit": "TFLOP/s",
-                          "frac": ach / tflops_peak, "ms": avg[j], "peak_kind": tpeak_kind,
-                          "algorithmic": st["flops_tensor"], "traffic": traffic.get(n)}
+            alg, unit, peak, pk, bound = st["flops_tensor"], "TFLOP/s", tflops_peak, tpeak_kind, "tensor"
+            scale = 1e12
         else:
-            alg = (st["unique_slots_rows"] * w.num_kv_heads * KV_BYTES_PER_SLOT_HEAD if n == "row_kernel"
+            alg = (slots[n] * w.num_kv_heads * KV_BYTES_PER_SLOT_HEAD if n in slots
                    else part_bytes // 2 + st["merge_rows"] * (128 * 2 + 4))
-            ach = alg / (avg[j] * 1e-3) / 1e9
-            kernels[n] = {"bound": "hbm", "achieved": ach, "peak": hbm_peak, "unit": "GB/s",
-                          "frac": ach / hbm_peak, "ms": avg[j], "peak_kind": peak_kind,
-                          "algorithmic": alg, "traffic": traffic.get(n)}
+            unit, peak, pk, bound, scale = "GB/s", hbm_peak, peak_kind, "hbm", 1e9
+        ach = alg / (avg[j] * 1e-3) / scale
+        kernels[n] = {"bound": bound, "achieved": ach, "peak": peak, "unit": unit,
+                      "frac": ach / peak, "ms": avg[j], "peak_kind": pk, "algorithmic": alg,
+                      "traffic": traffic.get(n), "ms_alone": alone[j],
+                      "frac_alone": alg / (alone[j] * 1e-3) / scale / peak if alone[j] > 0 else None}
     dom = max(kernels, key=lambda n: kernels[n]["ms"])
     roof = dict(kernels[dom])
     roof["kernel"] = dom
@@ -407,9 +414,13 @@ def run_ours(args):
             "roofline": roof,
             "kernels": kernels,
             "kernel_ms": {n: a for n, a in zip(names, avg)},
-            "per_kernel_pass": f"{Kk} steps, kernels run one after another (fork_attn_decode_timed)",
+            "kernel_ms_alone": {n: a for n, a in zip(names, alone)},
+            "per_kernel_timing": f"ms: CUDA events on each kernel's own stream in the timed steps "
+                                 f"(kernels concurrent); ms_alone: {Ka} further steps with the "
+                                 f"kernels one after another",
             "step_ms_min": min(step_ms), "step_ms_median": statistics.median(step_ms),
             "wall_s_timed_region": wall,
+            "tensor_ctas": st["tensor_ctas"],
             "gpu_launches": K * (int(st["num_items_row8"] > 0) + int(st["num_items_rows"] > st["num_items_row8"])
                                  + int(st["num_items_tensor"] > 0) + int(st["merge_rows"] > 0)),
             "flops_per_step": st["flops_rows"] + st["flops_tensor"],

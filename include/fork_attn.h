@@ -141,6 +141,10 @@ typedef struct {
     int64_t flops_rows;            /* algorithmic flops of the row kernel: per visible slot  */
     int64_t flops_tensor;          /* of a reader, 4 x 128 x (query rows) per KV head        */
     int64_t num_items_row8;        /* of num_items_rows: items with <= 8 rows (own kernel)   */
+    int64_t unique_slots_row8;     /* visible slots of the chunks that kernel reads          */
+    int64_t unique_slots_row32;    /* the same for the row kernel of up to 32 rows (a chunk  */
+                                   /* whose row groups go to both counts in both)            */
+    int64_t tensor_ctas;           /* persistent CTAs the tcgen05 kernel is launched with    */
 } fa_plan_stats;
 
 typedef struct fa_plan fa_plan; /* opaque; owned by the library */
@@ -182,21 +186,23 @@ int fork_attn_plan_upload(fa_plan *plan, void *dev_plan_buf, size_t plan_buf_byt
 int fork_attn_decode(const void *q, const void *k_pages, const void *v_pages,
                      const fa_plan *plan, void *out, float *lse, void *stream);
 
-/* The same decode with its three kernels run one after the other on `stream` (no helper
- * stream), for timing each kernel alone: if `events` [host] is not NULL it is an array of
- * 2*n_events cudaEvent_t handles (as void*) recorded on `stream` around each kernel launch:
- * [start_0, stop_0, start_1, stop_1, start_2, stop_2] for the row kernels (the one for
- * <= 8 rows, then the one for up to 32), the tcgen05 kernel
- * and the merge kernel (an absent kernel records start = stop).  n_events must be 0 or 3.
+/* The same decode with CUDA events recorded around each kernel, for timing the kernels.
+ * `events` [host] (may be NULL) is an array of 2*n_events cudaEvent_t handles (as void*):
+ * [start, stop] for the row kernel of at most 8 stacked rows, the row kernel of up to 32, the
+ * tcgen05 kernel and the merge kernel, in that order; each pair is recorded on the stream its
+ * kernel runs on (an absent kernel records start = stop).  n_events must be 0 or 4.
+ * concurrent != 0 runs the kernels exactly as fork_attn_decode does (below); concurrent == 0
+ * runs them one after the other on `stream`, so that each is timed alone.
  *
- * (fork_attn_decode itself, when a plan has work for both the row and the tcgen05 kernel,
- * runs the row kernel on a library-owned helper stream of the current device -- created on
- * that device's first such decode -- concurrently with the tcgen05 kernel on `stream`; the
- * two are joined by events before the merge, so the decode stays ordered on `stream` and
- * can be captured in a CUDA graph.) */
+ * fork_attn_decode itself, when a plan has work for more than one of the tcgen05 kernel and
+ * the two row kernels, runs them on three library-owned helper streams of the current device
+ * (created on that device's first such decode) that fork from `stream` and are joined back
+ * into it by events before the merge, so the decode stays ordered on `stream` and can be
+ * captured in a CUDA graph.  Concurrent decodes of one device take a host mutex around
+ * these launches. */
 int fork_attn_decode_timed(const void *q, const void *k_pages, const void *v_pages,
                            const fa_plan *plan, void *out, float *lse, void *stream,
-                           void **events, int32_t n_events);
+                           void **events, int32_t n_events, int32_t concurrent);
 
 /* Reads the plan's device error word on `stream` (synchronising it) into *device_error [host]
  * and clears it.  A non-zero word means a kernel gave up (an expired wait or a failed check)

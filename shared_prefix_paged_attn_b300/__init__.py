@@ -130,15 +130,21 @@ def fork_attn_decode(q, k_pages, v_pages, plan: Plan, out, lse, stream=None):
            "fork_attn_decode")
 
 
-def fork_attn_decode_timed(q, k_pages, v_pages, plan: Plan, out, lse, events, stream=None):
-    """events: 6 torch.cuda.Event(enable_timing=True), recorded around the three kernels."""
+def fork_attn_decode_timed(q, k_pages, v_pages, plan: Plan, out, lse, events, stream=None,
+                           concurrent=True):
+    """events: 8 torch.cuda.Event(enable_timing=True), [start, stop] around the row kernel of
+    <= 8 rows, the row kernel, the tcgen05 kernel and the merge, each on its kernel's stream;
+    concurrent=False runs the kernels one after another on `stream`."""
+    if len(events) != 8:
+        raise ValueError("fork_attn_decode_timed needs 8 events")
     for e in events:  # torch creates an event's handle on its first record
         if not e.cuda_event:
             e.record()
-    handles = (ctypes.c_void_p * 6)(*[ctypes.c_void_p(e.cuda_event) for e in events])
+    handles = (ctypes.c_void_p * 8)(*[ctypes.c_void_p(e.cuda_event) for e in events])
     _check(_lib.load().fork_attn_decode_timed(_ptr(q), _ptr(k_pages), _ptr(v_pages), plan.handle,
                                               _ptr(out), _ptr(lse), _stream_ptr(stream),
-                                              handles, 3), "fork_attn_decode_timed")
+                                              handles, 4, int(bool(concurrent))),
+           "fork_attn_decode_timed")
 
 
 def fork_attn_decode_static_scratch(q, k_pages, v_pages, plan: Plan, out, lse, stream=None):

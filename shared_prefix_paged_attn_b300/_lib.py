@@ -44,7 +44,8 @@ class FaPlanStats(ctypes.Structure):
                 ("partial_rows", c_int64), ("merge_rows", c_int64), ("total_q", c_int64),
                 ("unique_slots_rows", c_int64), ("unique_slots_tensor", c_int64),
                 ("flops_rows", c_int64), ("flops_tensor", c_int64),
-                ("num_items_row8", c_int64)]
+                ("num_items_row8", c_int64), ("unique_slots_row8", c_int64),
+                ("unique_slots_row32", c_int64), ("tensor_ctas", c_int64)]
 
 
 # name -> (restype, argtypes); every symbol declared in include/fork_attn.h
@@ -59,7 +60,8 @@ SIGNATURES = {
     "fork_attn_decode": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                    c_void_p]),
     "fork_attn_decode_timed": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
-                                         c_void_p, c_void_p, ctypes.POINTER(c_void_p), c_int32]),
+                                         c_void_p, c_void_p, ctypes.POINTER(c_void_p), c_int32,
+                                         c_int32]),
     "fork_attn_check": (c_int32, [c_void_p, ctypes.POINTER(c_int32), c_void_p]),
     "fork_attn_decode_static_scratch": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p,
                                                   c_void_p, c_void_p, c_void_p]),

@@ -173,9 +173,10 @@ Aux *aux_for_current_device() {
     return &aux[dev];
 }
 
-// Launches the decode kernels on `st`.  With `aux`, the tcgen05 and row kernels run on the
-// two helper streams concurrently, and the merge, on `st`, waits for both.  `events` (optional)
-// are recorded around each kernel on the stream it runs on.
+// Launches the decode kernels on `st`.  With `aux`, the tcgen05 kernel and the two row kernels
+// run on three helper streams concurrently, and the merge, on `st`, waits for all of them.
+// `events` (optional, 8 handles) are recorded around each kernel on the stream it runs on, in
+// the order row8, row, tcgen05, merge.
 int launch_all(const fa::DecodeParams &p, const fa_plan *plan, cudaStream_t st, void **events, Aux *aux) {
     bool ev_ok = true;
     auto rec = [&](int i, cudaStream_t s) {
@@ -194,17 +195,18 @@ int launch_all(const fa::DecodeParams &p, const fa_plan *plan, cudaStream_t st, 
     }
     cudaStream_t ts = both ? aux->tc_stream : st, rs = both ? aux->row_stream : st;
     cudaStream_t r8s = both ? aux->row8_stream : st;
-    rec(2, ts);
+    rec(4, ts);
     if (p.n_items_tc > 0)
         fa::tck::tc_kernel<<<p.tc_ctas, fa::tck::kThreads, fa::tck::kSmemBytes, ts>>>(p);
-    rec(3, ts);
-    // the per-kernel events (sequential decode only) span both row kernels
-    rec(0, rs);
+    rec(5, ts);
+    rec(0, r8s);
     if (p.n_items_r8 > 0)
         fa::r8k::row8_kernel<<<p.n_items_r8, fa::r8k::kThreads, fa::r8k::kSmemBytes, r8s>>>(p);
+    rec(1, r8s);
+    rec(2, rs);
     if (p.n_items > 0)
         fa::rowk::row_kernel<<<p.n_items, fa::rowk::kThreads, fa::rowk::kSmemBytes, rs>>>(p);
-    rec(1, rs);
+    rec(3, rs);
     if (both) {
         if (cudaEventRecord(aux->join_tc, aux->tc_stream) != cudaSuccess ||
             cudaEventRecord(aux->join_row, aux->row_stream) != cudaSuccess ||
@@ -214,13 +216,13 @@ int launch_all(const fa::DecodeParams &p, const fa_plan *plan, cudaStream_t st, 
             cudaStreamWaitEvent(st, aux->join_row8, 0) != cudaSuccess)
             return FA_ERR_CUDA;
     }
-    rec(4, st);
+    rec(6, st);
     if (needs_merge(plan)) {
         const int64_t threads = int64_t(p.total_rows) * 32;
         const int blocks = int((threads + fa::mergek::kThreads - 1) / fa::mergek::kThreads);
         fa::mergek::merge_kernel<<<blocks, fa::mergek::kThreads, 0, st>>>(p);
     }
-    rec(5, st);
+    rec(7, st);
     const bool launched = cudaGetLastError() == cudaSuccess;
     if (!ev_ok) return FA_ERR_INVALID;
     return launched ? FA_OK : FA_ERR_CUDA;
@@ -251,19 +253,24 @@ extern "C" int fork_attn_plan_upload(fa_plan *plan, void *dev_plan_buf, size_t p
 
 extern "C" int fork_attn_decode_timed(const void *q, const void *k_pages, const void *v_pages,
                                       const fa_plan *plan, void *out, float *lse, void *stream,
-                                      void **events, int32_t n_events) {
+                                      void **events, int32_t n_events, int32_t concurrent) {
     if (!plan || !q || !k_pages || !v_pages || !out || !lse) return FA_ERR_NULL;
     if (!plan->uploaded) return FA_ERR_NOT_UPLOADED;
     if (!aligned(q, 16) || !aligned(k_pages, 16) || !aligned(v_pages, 16) || !aligned(out, 16) ||
         !aligned(lse, 16))
         return FA_ERR_ALIGN;
-    if (events && n_events != 3) return FA_ERR_INVALID;
+    if (events && n_events != 4) return FA_ERR_INVALID;
     int rc = set_smem_attr();
     if (rc != FA_OK) return rc;
     fa::DecodeParams p;
     rc = fill_params(plan, q, k_pages, v_pages, out, lse, plan->dev_scratch, p);
     if (rc != FA_OK) return rc;
-    return launch_all(p, plan, static_cast<cudaStream_t>(stream), events, nullptr);  // sequential
+    Aux *aux = nullptr;
+    if (concurrent) {
+        aux = aux_for_current_device();
+        if (!aux) return FA_ERR_CUDA;
+    }
+    return launch_all(p, plan, static_cast<cudaStream_t>(stream), events, aux);
 }
 
 extern "C" int fork_attn_decode(const void *q, const void *k_pages, const void *v_pages,

@@ -281,6 +281,7 @@ int build_plan(Input &in, const fa_plan_opts &opts, fa_plan *plan) {
 
     const int32_t tmin = opts.tensor_min_rows < 0 ? 0 : (opts.tensor_min_rows > 0 ? opts.tensor_min_rows : 64);
     std::vector<char> chunk_tc;  // per chunk: its items go to the tcgen05 kernel
+    std::vector<int64_t> chunk_slots;  // per chunk: visible slots of its pages (any reader)
     std::vector<int32_t> occ_count(B, 0);
     for (const auto &run : runs) {
         const int32_t g0 = run[0];
@@ -308,11 +309,13 @@ int build_plan(Input &in, const fa_plan_opts &opts, fa_plan *plan) {
             ch.n_pages = int32_t(len);
             ch.occ_off = int32_t(em.occs.size());
             ch.n_occ = n_read;
+            int64_t slots_c = 0;
             for (int64_t k = 0; k < len; ++k) {
                 const int32_t g = run[pos + k];
                 em.chunk_pages.push_back(bd.recs[bd.by_page[bd.group_start[g]]].page);
                 st.unique_visible_slots += __builtin_popcount(bd.group_union[g]);
                 (tc_run ? st.unique_slots_tensor : st.unique_slots_rows) += __builtin_popcount(bd.group_union[g]);
+                slots_c += __builtin_popcount(bd.group_union[g]);
                 st.touched_pages += 1;
                 for (int32_t t = 0; t < n_read; ++t) {
                     const Rec &rd = bd.recs[bd.by_page[bd.group_start[g] + t]];
@@ -348,6 +351,7 @@ int build_plan(Input &in, const fa_plan_opts &opts, fa_plan *plan) {
             }
             em.chunks.push_back(ch);
             chunk_tc.push_back(tc_run ? 1 : 0);
+            chunk_slots.push_back(slots_c);
             pos += len;
         }
     }
@@ -414,6 +418,12 @@ int build_plan(Input &in, const fa_plan_opts &opts, fa_plan *plan) {
             }
         }
         if (cur_rows) groups.push_back({cur_off, cur_rows});
+        if (!tc) {  // the visible slots each row kernel must read (once per launch)
+            bool r8 = false, r32 = false;
+            for (const auto &gr : groups) (gr.second <= 8 ? r8 : r32) = true;
+            if (r8) st.unique_slots_row8 += chunk_slots[c];
+            if (r32) st.unique_slots_row32 += chunk_slots[c];
+        }
         for (int32_t h = 0; h < Hkv; ++h) {
             for (size_t gi = 0; gi < groups.size(); ++gi) {
                 fa::Item it;
@@ -461,6 +471,7 @@ int build_plan(Input &in, const fa_plan_opts &opts, fa_plan *plan) {
         if (opts.reserved[0] > 0) n = opts.reserved[0];
         n = std::max(1, std::min(n, sms));
         plan->tc_ctas = int32_t(std::min<int64_t>(n, std::max<size_t>(em.items_tc.size(), 1)));
+        st.tensor_ctas = em.items_tc.empty() ? 0 : plan->tc_ctas;
     }
 
     st.num_chunks = int64_t(em.chunks.size());

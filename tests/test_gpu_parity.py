@@ -176,3 +176,40 @@ def test_small_configs_kernel_split(cfg, tmin):
     out, lse = gpu_decode(w, fa.FA_F32, tensor_min_rows=tmin)
     ref_out, ref_lse = oracle.fork_attn(w)
     assert_parity(out, lse, ref_out, ref_lse, f"config {cfg} tmin {tmin}")
+
+
+@pytest.mark.parametrize("cfg", [3, 5])
+def test_tensor_cta_count_does_not_change_results(cfg):
+    # the persistent tcgen05 CTAs take items from a queue: whichever CTA runs an item, and
+    # however many run, every output bit is the same (and the queue resets between decodes)
+    w = W.make(cfg, small=True)
+    base = gpu_decode(w, tensor_min_rows=1)
+    for n in (1, 3, 148, 0):
+        got = gpu_decode(w, tensor_min_rows=1, tensor_ctas=n)
+        assert np.array_equal(base[0], got[0]) and np.array_equal(base[1], got[1]), n
+    ref_out, ref_lse = oracle.fork_attn(w)
+    assert_parity(*base, ref_out, ref_lse)
+
+
+def test_timed_decode_matches_decode_bitwise():
+    w = W.make(3, small=True)
+    dev = torch.device("cuda")
+    q, k, v = w.q.to(dev), w.k_pages.to(dev), w.v_pages.to(dev)
+    run = fa.ForkAttention(w, out_dtype=fa.FA_F32, tensor_min_rows=16)
+    st = run.plan.stats()
+    base_out, base_lse = (x.clone() for x in run(q, k, v))
+    for concurrent in (True, False):
+        for _ in range(2):  # twice: the tcgen05 work queue must be reset by the first
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(8)]
+            run.out.zero_()
+            run.lse.zero_()
+            fa.fork_attn_decode_timed(q, k, v, run.plan, run.out, run.lse, ev,
+                                      concurrent=concurrent)
+            torch.cuda.synchronize()
+            assert fa.fork_attn_check(run.plan) == 0
+            assert torch.equal(run.out, base_out) and torch.equal(run.lse, base_lse)
+            ms = [ev[2 * j].elapsed_time(ev[2 * j + 1]) for j in range(4)]
+            present = [st["num_items_row8"] > 0, st["num_items_rows"] > st["num_items_row8"],
+                       st["num_items_tensor"] > 0, st["merge_rows"] > 0]
+            for t, there in zip(ms, present):
+                assert (t > 0) if there else (0 <= t < 0.005), (ms, present)

@@ -143,3 +143,23 @@ def test_flop_counters_match_the_definition(cfg):
                for b in range(w.num_branches)) * G * w.num_kv_heads * 4 * 128
     assert st["flops_rows"] + st["flops_tensor"] == want
     assert st["flops_tensor"] > 0 or cfg == 1
+
+
+@pytest.mark.parametrize("cfg", [1, 2, 3, 4, 5])
+def test_per_kernel_slot_counters(cfg):
+    # each row kernel's count covers the chunks it reads; together they cover every row chunk,
+    # a chunk split between both kernels counting in both
+    w = W.make(cfg, small=True, values=False)
+    for tmin in (0, -1):
+        st = fa.plan_for(w, tensor_min_rows=tmin).stats()
+        r8, r32, rows = st["unique_slots_row8"], st["unique_slots_row32"], st["unique_slots_rows"]
+        assert max(r8, r32) <= rows <= r8 + r32
+        assert (r8 > 0) == (st["num_items_row8"] > 0)
+        assert (r32 > 0) == (st["num_items_rows"] > st["num_items_row8"])
+        assert rows + st["unique_slots_tensor"] == st["unique_visible_slots"]
+        if st["num_items_tensor"]:
+            assert 1 <= st["tensor_ctas"] <= min(148, st["num_items_tensor"])
+        else:
+            assert st["tensor_ctas"] == 0
+    st = fa.plan_for(w, tensor_min_rows=1, tensor_ctas=3).stats()
+    assert st["tensor_ctas"] == min(3, st["num_items_tensor"])
