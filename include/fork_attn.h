@@ -116,8 +116,11 @@ typedef struct {
     int32_t num_sms;        /* SMs to plan for (0 = 148)                                     */
     int32_t tensor_min_rows;/* reader-set rows at which a run goes to the tcgen05 kernel    */
                             /* (0 = default; < 0 = never)                                    */
-    int32_t reserved[5];    /* [0] > 0: persistent CTAs of the tcgen05 kernel (0 = from the  */
-                            /* planner's split of SMs between it and the row kernels)        */
+    int32_t tensor_ctas;    /* persistent CTAs of the tcgen05 kernel (0 = from the planner's */
+                            /* split of SMs between it and the row kernels)                  */
+    int32_t tensor_chunk_pages; /* max pages per tcgen05 chunk, rounded up to whole 8-page   */
+                            /* tiles (0 = chosen by the planner)                             */
+    int32_t reserved[3];    /* must be 0                                                     */
 } fa_plan_opts;
 
 /* Counters of a plan, for measurement.  unique_visible_slots: distinct physical token slots
@@ -152,7 +155,8 @@ typedef struct fa_plan fa_plan; /* opaque; owned by the library */
 /* Builds a plan on the host: validates dims and descriptor, finds runs of physical pages
  * with the same reader set, skips pages no reader sees, cuts runs into chunks, assigns
  * partial-result rows and packs per-chunk visibility words.  Errors: FA_ERR_NULL,
- * FA_ERR_INVALID (bad CSR, n_q outside [1, n_b], empty branch, bad scale/out_dtype),
+ * FA_ERR_INVALID (bad CSR, n_q outside [1, n_b], empty branch, bad scale/out_dtype, a
+ * negative planner knob or a non-zero reserved field),
  * FA_ERR_RANGE (segment id, page offset or page id out of range, bit array too short),
  * FA_ERR_UNSUPPORTED (head_dim != 128, page_size != 16, Hq % Hkv != 0, G > 32),
  * FA_ERR_NOMEM.  *out_plan is set only on FA_OK. */

@@ -87,7 +87,7 @@ def fork_attn_plan_create(num_q_heads, num_kv_heads, page_ids, segs, branch_seg_
                           branch_segs, num_pages_pool, branch_q_off=None, vis_bits=None,
                           vis_word_off=None, scale=None, out_dtype=FA_BF16, head_dim=128,
                           page_size=16, chunk_pages=0, num_sms=0, tensor_min_rows=0,
-                          tensor_ctas=0) -> Plan:
+                          tensor_ctas=0, tensor_chunk_pages=0) -> Plan:
     """fork_attn_plan_create over host (numpy) descriptor arrays."""
     keep = []
 
@@ -116,7 +116,7 @@ def fork_attn_plan_create(num_q_heads, num_kv_heads, page_ids, segs, branch_seg_
     desc.num_pages_pool = int(num_pages_pool)
     opts = FaPlanOpts()
     opts.chunk_pages, opts.num_sms, opts.tensor_min_rows = int(chunk_pages), int(num_sms), int(tensor_min_rows)
-    opts.reserved[0] = int(tensor_ctas)  # persistent CTAs of the tcgen05 kernel (0 = planner's choice)
+    opts.tensor_ctas, opts.tensor_chunk_pages = int(tensor_ctas), int(tensor_chunk_pages)
     handle = ctypes.c_void_p()
     _check(_lib.load().fork_attn_plan_create(ctypes.byref(dims), ctypes.byref(desc),
                                              ctypes.byref(opts), ctypes.byref(handle)),

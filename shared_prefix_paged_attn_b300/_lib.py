@@ -33,7 +33,8 @@ class FaDesc(ctypes.Structure):
 
 class FaPlanOpts(ctypes.Structure):
     _fields_ = [("chunk_pages", c_int32), ("num_sms", c_int32), ("tensor_min_rows", c_int32),
-                ("reserved", c_int32 * 5)]
+                ("tensor_ctas", c_int32), ("tensor_chunk_pages", c_int32),
+                ("reserved", c_int32 * 3)]
 
 
 class FaPlanStats(ctypes.Structure):

@@ -297,6 +297,8 @@ int build_plan(Input &in, const fa_plan_opts &opts, fa_plan *plan) {
         if (opts.chunk_pages > 0) target = opts.chunk_pages;
         target = std::min<int64_t>(target, fa::kMaxChunkPages);
         const bool tc_run = tmin > 0 && rows >= tmin;
+        if (tc_run && opts.tensor_chunk_pages > 0)
+            target = std::min<int64_t>(fa::kMaxChunkPages, ceil_div(opts.tensor_chunk_pages, 8) * 8);
         const int64_t n = int64_t(run.size());
         const int64_t n_ch = std::max<int64_t>(1, ceil_div(n, target));
         // tcgen05 chunks are whole 128-token tiles (8 pages) except the last one of a run
@@ -458,7 +460,7 @@ int build_plan(Input &in, const fa_plan_opts &opts, fa_plan *plan) {
     // the private runs on the others.  Its work is compute (about 1.14 us of one SM per
     // 128-token tile of one 128-row M tile), theirs is memory (about 130 GB/s per SM they
     // hold); the split gives each side SMs in proportion to its SM time.  (Both constants are
-    // fitted to B300 sweeps of the split; fa_plan_opts.reserved[0] > 0 overrides the count.)
+    // fitted to B300 sweeps of the split; fa_plan_opts.tensor_ctas > 0 overrides the count.)
     {
         double w_tc = 0.0;
         for (const fa::Item &it : em.items_tc) {
@@ -468,7 +470,7 @@ int build_plan(Input &in, const fa_plan_opts &opts, fa_plan *plan) {
         const double w_row = double(st.kv_bytes_rows) / 130e9;
         const int sms = opts.num_sms > 0 ? opts.num_sms : 148;
         int n = w_tc + w_row > 0.0 ? int(std::lround(sms * w_tc / (w_tc + w_row))) : sms;
-        if (opts.reserved[0] > 0) n = opts.reserved[0];
+        if (opts.tensor_ctas > 0) n = opts.tensor_ctas;
         n = std::max(1, std::min(n, sms));
         plan->tc_ctas = int32_t(std::min<int64_t>(n, std::max<size_t>(em.items_tc.size(), 1)));
         st.tensor_ctas = em.items_tc.empty() ? 0 : plan->tc_ctas;
@@ -539,6 +541,9 @@ extern "C" int fork_attn_plan_create(const fa_dims *dims, const fa_desc *desc,
         fa_plan_opts o;
         std::memset(&o, 0, sizeof o);
         if (opts) o = *opts;
+        if (o.chunk_pages < 0 || o.num_sms < 0 || o.tensor_ctas < 0 || o.tensor_chunk_pages < 0 ||
+            o.reserved[0] || o.reserved[1] || o.reserved[2])
+            return FA_ERR_INVALID;
         fa_plan *p = new fa_plan();
         p->dims = *dims;
         p->G = in.G;

@@ -83,6 +83,30 @@ def test_validation_errors():
         assert _plan_rc(variant(vis_bits=good.vis_bits[:1])) == -4
     for hq, hkv, rc in ((6, 4, -3), (64, 1, -3)):
         assert _plan_rc(variant(num_q_heads=hq, num_kv_heads=hkv)) == rc
+    for knob in ("chunk_pages", "num_sms", "tensor_ctas", "tensor_chunk_pages"):
+        assert _plan_rc(good, **{knob: -1}) == -2
+
+
+def test_reserved_planner_fields_must_be_zero():
+    w = W.config1(values=False)
+    lib = _lib.load()
+    dims = _lib.FaDims(8, 2, 128, 16, 1.0 / np.sqrt(128), fa.FA_BF16)
+    keep = [np.ascontiguousarray(x) for x in (w.page_ids, w.segs, w.branch_seg_off, w.branch_segs)]
+    desc = _lib.FaDesc()
+    desc.page_ids, desc.num_page_ids = keep[0].ctypes.data, len(w.page_ids)
+    desc.segs, desc.num_segs = keep[1].ctypes.data, len(w.segs)
+    desc.branch_seg_off, desc.branch_segs = keep[2].ctypes.data, keep[3].ctypes.data
+    desc.num_branches = len(w.branch_seg_off) - 1
+    desc.num_pages_pool = w.num_pages_pool
+    handle = ctypes.c_void_p()
+    for i in range(4):
+        opts = _lib.FaPlanOpts()
+        if i < 3:
+            opts.reserved[i] = 1
+        rc = lib.fork_attn_plan_create(ctypes.byref(dims), ctypes.byref(desc), ctypes.byref(opts),
+                                       ctypes.byref(handle))
+        assert rc == (-2 if i < 3 else 0)
+    assert lib.fork_attn_plan_destroy(handle) == 0
 
 
 def test_unsupported_dims_and_nulls():
