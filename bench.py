@@ -280,12 +280,11 @@ def run_ours(args):
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     q, k, v = w.q, w.k_pages, w.v_pages
 
-    def step(events=None, concurrent=True):
+    def step(events=None):
         if events is None:
             fa.fork_attn_decode(q, k, v, run.plan, run.out, run.lse, stream)
         else:
-            fa.fork_attn_decode_timed(q, k, v, run.plan, run.out, run.lse, events, stream,
-                                      concurrent=concurrent)
+            fa.fork_attn_decode_timed(q, k, v, run.plan, run.out, run.lse, events, stream)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -319,35 +318,20 @@ def run_ours(args):
     value = unique_bytes * world / (ms_max * 1e-3) / 1e9
     bq_s = w.total_q * world / (ms_max * 1e-3)
 
-    # Per-kernel durations: the same decode, kernels concurrent on their helper streams as in
-    # the timed region, with CUDA events recorded around each kernel on the stream it runs
-    # on.  Those event records lengthen the step (their cost is reported beside it), so they
-    # are kept out of the timed region above and taken in this second pass of Kk steps.
+    # Per-kernel durations: inside the decode the kernels overlap on one stream (the row
+    # kernels are programmatic dependent launches beside the tcgen05 kernel), where a CUDA
+    # event between two of them would serialise them.  So each kernel is timed alone, with
+    # CUDA events on the launching stream, in Kk further steps of the same decode with its
+    # kernels one after another (fork_attn_decode_timed), L2 flushed before every step.
     Kk = min(K, 100)
-    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * len(names))] for _ in range(Kk)]
-    kst = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(Kk)]
+    aev = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * len(names))] for _ in range(Kk)]
     for i in range(Kk):
         flush.zero_()
-        kst[i][0].record(stream)
-        step(kev[i])
-        kst[i][1].record(stream)
-    torch.cuda.synchronize(dev)
-    assert fa.fork_attn_check(run.plan, stream) == 0, "device error word set in the per-kernel pass"
-    avg = [sum(kev[i][2 * j].elapsed_time(kev[i][2 * j + 1]) for i in range(Kk)) / Kk
-           for j in range(len(names))]
-    step_ms_events = sum(a.elapsed_time(b) for a, b in kst) / Kk
-
-    # For comparison, each kernel alone: the same decode with its kernels one after another
-    # on `stream` (L2 flushed before every step as above).
-    Ka = min(K, 50)
-    aev = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * len(names))] for _ in range(Ka)]
-    for i in range(Ka):
-        flush.zero_()
-        step(aev[i], concurrent=False)
+        step(aev[i])
     torch.cuda.synchronize(dev)
     assert fa.fork_attn_check(run.plan, stream) == 0, "device error word set in the one-by-one pass"
-    alone = [sum(aev[i][2 * j].elapsed_time(aev[i][2 * j + 1]) for i in range(Ka)) / Ka
-             for j in range(len(names))]
+    avg = [sum(aev[i][2 * j].elapsed_time(aev[i][2 * j + 1]) for i in range(Kk)) / Kk
+           for j in range(len(names))]
 
     hbm_peak, peak_kind = peaks()
     tflops_peak, tpeak_kind = tensor_peak()
@@ -370,8 +354,7 @@ def run_ours(args):
         ach = alg / (avg[j] * 1e-3) / scale
         kernels[n] = {"bound": bound, "achieved": ach, "peak": peak, "unit": unit,
                       "frac": ach / peak, "ms": avg[j], "peak_kind": pk, "algorithmic": alg,
-                      "traffic": traffic.get(n), "ms_alone": alone[j],
-                      "frac_alone": alg / (alone[j] * 1e-3) / scale / peak if alone[j] > 0 else None}
+                      "traffic": traffic.get(n)}
     dom = max(kernels, key=lambda n: kernels[n]["ms"])
     roof = dict(kernels[dom])
     roof["kernel"] = dom
@@ -429,11 +412,9 @@ def run_ours(args):
             "roofline": roof,
             "kernels": kernels,
             "kernel_ms": {n: a for n, a, p in zip(names, avg, present) if p},
-            "kernel_ms_alone": {n: a for n, a, p in zip(names, alone, present) if p},
-            "per_kernel_timing": f"ms: CUDA events on each kernel's own stream, {Kk} steps of the "
-                                 f"same concurrent decode after the timed region (with those events "
-                                 f"a step took {step_ms_events:.4f} ms); ms_alone: {Ka} steps with "
-                                 f"the kernels one after another",
+            "per_kernel_timing": f"each kernel alone: CUDA events on the launching stream over {Kk} "
+                                 f"steps of the decode with its kernels one after another; in the "
+                                 f"timed region they overlap",
             "step_ms_min": min(step_ms), "step_ms_median": statistics.median(step_ms),
             "wall_s_timed_region": wall,
             "tensor_ctas": st["tensor_ctas"],

@@ -190,23 +190,21 @@ int fork_attn_plan_upload(fa_plan *plan, void *dev_plan_buf, size_t plan_buf_byt
 int fork_attn_decode(const void *q, const void *k_pages, const void *v_pages,
                      const fa_plan *plan, void *out, float *lse, void *stream);
 
-/* The same decode with CUDA events recorded around each kernel, for timing the kernels.
- * `events` [host] (may be NULL) is an array of 2*n_events cudaEvent_t handles (as void*):
- * [start, stop] for the row kernel of at most 8 stacked rows, the row kernel of up to 32, the
- * tcgen05 kernel and the merge kernel, in that order; each pair is recorded on the stream its
- * kernel runs on (an absent kernel records start = stop).  n_events must be 0 or 4.
- * concurrent != 0 runs the kernels exactly as fork_attn_decode does (below); concurrent == 0
- * runs them one after the other on `stream`, so that each is timed alone.
+/* The same decode with its kernels run one after the other on `stream`, each timed alone:
+ * `events` [host] (may be NULL) is an array of 2*n_events cudaEvent_t handles (as void*),
+ * [start, stop] recorded on `stream` around the row kernel of at most 8 stacked rows, the row
+ * kernel of up to 32, the tcgen05 kernel and the merge kernel, in that order (an absent kernel
+ * records start = stop).  n_events must be 0 or 4.
  *
- * fork_attn_decode itself, when a plan has work for more than one of the tcgen05 kernel and
- * the two row kernels, runs them on three library-owned helper streams of the current device
- * (created on that device's first such decode) that fork from `stream` and are joined back
- * into it by events before the merge, so the decode stays ordered on `stream` and can be
- * captured in a CUDA graph.  Concurrent decodes of one device take a host mutex around
- * these launches. */
+ * fork_attn_decode itself runs the kernels overlapped, all on `stream`: the tcgen05 kernel
+ * first, then the row kernels as programmatic dependent launches (they start once every
+ * tcgen05 CTA has started, and take the SMs it leaves and frees), then the merge as an
+ * ordinary launch after all of them.  No helper stream or event is involved, so a decode can
+ * be captured into a CUDA graph; an event recorded between those kernels would only order
+ * them, which is why this call runs them one by one instead. */
 int fork_attn_decode_timed(const void *q, const void *k_pages, const void *v_pages,
                            const fa_plan *plan, void *out, float *lse, void *stream,
-                           void **events, int32_t n_events, int32_t concurrent);
+                           void **events, int32_t n_events);
 
 /* Reads the plan's device error word on `stream` (synchronising it) into *device_error [host]
  * and clears it.  A non-zero word means a kernel gave up (an expired wait or a failed check)

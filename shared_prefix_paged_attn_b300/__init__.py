@@ -130,11 +130,10 @@ def fork_attn_decode(q, k_pages, v_pages, plan: Plan, out, lse, stream=None):
            "fork_attn_decode")
 
 
-def fork_attn_decode_timed(q, k_pages, v_pages, plan: Plan, out, lse, events, stream=None,
-                           concurrent=True):
-    """events: 8 torch.cuda.Event(enable_timing=True), [start, stop] around the row kernel of
-    <= 8 rows, the row kernel, the tcgen05 kernel and the merge, each on its kernel's stream;
-    concurrent=False runs the kernels one after another on `stream`."""
+def fork_attn_decode_timed(q, k_pages, v_pages, plan: Plan, out, lse, events, stream=None):
+    """The decode with its kernels one after another on `stream`; events: 8
+    torch.cuda.Event(enable_timing=True), [start, stop] around the row kernel of <= 8 rows, the
+    row kernel, the tcgen05 kernel and the merge."""
     if len(events) != 8:
         raise ValueError("fork_attn_decode_timed needs 8 events")
     for e in events:  # torch creates an event's handle on its first record
@@ -143,8 +142,7 @@ def fork_attn_decode_timed(q, k_pages, v_pages, plan: Plan, out, lse, events, st
     handles = (ctypes.c_void_p * 8)(*[ctypes.c_void_p(e.cuda_event) for e in events])
     _check(_lib.load().fork_attn_decode_timed(_ptr(q), _ptr(k_pages), _ptr(v_pages), plan.handle,
                                               _ptr(out), _ptr(lse), _stream_ptr(stream),
-                                              handles, 4, int(bool(concurrent))),
-           "fork_attn_decode_timed")
+                                              handles, 4), "fork_attn_decode_timed")
 
 
 def fork_attn_decode_static_scratch(q, k_pages, v_pages, plan: Plan, out, lse, stream=None):

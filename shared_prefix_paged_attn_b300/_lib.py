@@ -61,8 +61,7 @@ SIGNATURES = {
     "fork_attn_decode": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                    c_void_p]),
     "fork_attn_decode_timed": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
-                                         c_void_p, c_void_p, ctypes.POINTER(c_void_p), c_int32,
-                                         c_int32]),
+                                         c_void_p, c_void_p, ctypes.POINTER(c_void_p), c_int32]),
     "fork_attn_check": (c_int32, [c_void_p, ctypes.POINTER(c_int32), c_void_p]),
     "fork_attn_decode_static_scratch": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p,
                                                   c_void_p, c_void_p, c_void_p]),

@@ -68,7 +68,7 @@ bool encode_pages_whole(CUtensorMap *map, const void *pages, int64_t pool, int32
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 int set_smem_attr() {
-    // once per device: the row kernel needs more than the default 48 KiB of dynamic smem
+    // once per device: the kernels need more than the default 48 KiB of dynamic smem
     static std::mutex mu;
     static bool done[128] = {false};
     int dev = 0;
@@ -99,6 +99,7 @@ int fill_params(const fa_plan *plan, const void *q, const void *k_pages, const v
     std::memset(&p, 0, sizeof p);
     if (!encode_pages(&p.kmap, k_pages, plan->num_pages_pool, plan->dims.num_kv_heads) ||
         !encode_pages(&p.vmap, v_pages, plan->num_pages_pool, plan->dims.num_kv_heads) ||
+        !encode_pages_whole(&p.kmap_page, k_pages, plan->num_pages_pool, plan->dims.num_kv_heads) ||
         !encode_pages_whole(&p.vmap_page, v_pages, plan->num_pages_pool, plan->dims.num_kv_heads))
         return FA_ERR_CUDA;
     const fa::Layout &L = plan->lay;
@@ -137,93 +138,58 @@ int fill_params(const fa_plan *plan, const void *q, const void *k_pages, const v
 
 bool needs_merge(const fa_plan *plan) { return plan->stats.merge_rows > 0; }
 
-// Per-device helper streams and events that let the row kernel and the tcgen05 kernel run at
-// the same time.  The tcgen05 kernel (one CTA per SM, the longer critical path) runs on the
-// highest-priority stream so that freed SMs take its CTAs first; the row kernel's CTAs fill
-// whatever is left.  Created on a device's first concurrent decode; the fork/join is plain
-// stream work (event record + stream wait), so a decode can be captured into a CUDA graph.
-struct Aux {
-    cudaStream_t tc_stream = nullptr;   // highest priority: the tcgen05 kernel's CTAs go first
-    cudaStream_t row_stream = nullptr;  // lowest priority: row CTAs fill the SMs left over
-    cudaStream_t row8_stream = nullptr;  // lowest priority, beside the other row kernel
-    cudaEvent_t fork = nullptr, join_tc = nullptr, join_row = nullptr, join_row8 = nullptr;
-    std::mutex mu;  // the events are shared by every decode on the device
-};
-
-Aux *aux_for_current_device() {
-    static std::mutex mu;
-    static Aux aux[128];
-    static bool ready[128] = {false};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return nullptr;
-    std::lock_guard<std::mutex> lk(mu);
-    if (!ready[dev]) {
-        int least = 0, greatest = 0;
-        if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess ||
-            cudaStreamCreateWithPriority(&aux[dev].tc_stream, cudaStreamNonBlocking, greatest) != cudaSuccess ||
-            cudaStreamCreateWithPriority(&aux[dev].row_stream, cudaStreamNonBlocking, least) != cudaSuccess ||
-            cudaStreamCreateWithPriority(&aux[dev].row8_stream, cudaStreamNonBlocking, least) != cudaSuccess ||
-            cudaEventCreateWithFlags(&aux[dev].join_row8, cudaEventDisableTiming) != cudaSuccess ||
-            cudaEventCreateWithFlags(&aux[dev].fork, cudaEventDisableTiming) != cudaSuccess ||
-            cudaEventCreateWithFlags(&aux[dev].join_tc, cudaEventDisableTiming) != cudaSuccess ||
-            cudaEventCreateWithFlags(&aux[dev].join_row, cudaEventDisableTiming) != cudaSuccess)
-            return nullptr;
-        ready[dev] = true;
-    }
-    return &aux[dev];
-}
-
-// Launches the decode kernels on `st`.  With `aux`, the tcgen05 kernel and the two row kernels
-// run on three helper streams concurrently, and the merge, on `st`, waits for all of them.
-// `events` (optional, 8 handles) are recorded around each kernel on the stream it runs on, in
-// the order row8, row, tcgen05, merge.
-int launch_all(const fa::DecodeParams &p, const fa_plan *plan, cudaStream_t st, void **events, Aux *aux) {
+// Launches the decode kernels on `st`.  chain = true (fork_attn_decode): the tcgen05 kernel
+// first, then the row kernels as programmatic dependent launches -- each CTA of the kernel
+// before releases its dependents as soon as it starts, so the row kernels' CTAs are placed
+// only after every persistent tcgen05 CTA holds its SM, and fill the SMs left over and those
+// the tcgen05 CTAs free -- then the merge as an ordinary launch, which waits for all of them.
+// The row kernels do not read what the tcgen05 kernel writes.  chain = false: the kernels
+// one after another, with `events` (optional, 8 handles) recorded around each of them in the
+// order row8, row, tcgen05, merge.
+int launch_all(const fa::DecodeParams &p, const fa_plan *plan, cudaStream_t st, void **events, bool chain) {
     bool ev_ok = true;
-    auto rec = [&](int i, cudaStream_t s) {
-        if (events) ev_ok = ev_ok && cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s) == cudaSuccess;
+    auto rec = [&](int i) {
+        if (events) ev_ok = ev_ok && cudaEventRecord(static_cast<cudaEvent_t>(events[i]), st) == cudaSuccess;
     };
-    const int kinds = int(p.n_items > 0) + int(p.n_items_r8 > 0) + int(p.n_items_tc > 0);
-    const bool both = aux && kinds > 1;
-    std::unique_lock<std::mutex> lk;
-    if (both) {
-        lk = std::unique_lock<std::mutex>(aux->mu);
-        if (cudaEventRecord(aux->fork, st) != cudaSuccess ||
-            cudaStreamWaitEvent(aux->tc_stream, aux->fork, 0) != cudaSuccess ||
-            cudaStreamWaitEvent(aux->row_stream, aux->fork, 0) != cudaSuccess ||
-            cudaStreamWaitEvent(aux->row8_stream, aux->fork, 0) != cudaSuccess)
-            return FA_ERR_CUDA;
+    bool after_kernel = false;  // a kernel of this decode precedes the next launch on `st`
+    auto launch = [&](auto kernel, int grid, int threads, size_t smem) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(unsigned(grid));
+        cfg.blockDim = dim3(unsigned(threads));
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = chain && after_kernel ? 1 : 0;
+        after_kernel = true;
+        return cudaLaunchKernelEx(&cfg, kernel, p) == cudaSuccess;
+    };
+    bool ok = true;
+    if (chain) {
+        if (p.n_items_tc > 0) ok = ok && launch(fa::tck::tc_kernel, p.tc_ctas, fa::tck::kThreads, fa::tck::kSmemBytes);
+        if (p.n_items_r8 > 0) ok = ok && launch(fa::r8k::row8_kernel, p.n_items_r8, fa::r8k::kThreads, fa::r8k::kSmemBytes);
+        if (p.n_items > 0) ok = ok && launch(fa::rowk::row_kernel, p.n_items, fa::rowk::kThreads, fa::rowk::kSmemBytes);
+    } else {
+        rec(0);
+        if (p.n_items_r8 > 0) ok = ok && launch(fa::r8k::row8_kernel, p.n_items_r8, fa::r8k::kThreads, fa::r8k::kSmemBytes);
+        rec(1);
+        rec(2);
+        if (p.n_items > 0) ok = ok && launch(fa::rowk::row_kernel, p.n_items, fa::rowk::kThreads, fa::rowk::kSmemBytes);
+        rec(3);
+        rec(4);
+        if (p.n_items_tc > 0) ok = ok && launch(fa::tck::tc_kernel, p.tc_ctas, fa::tck::kThreads, fa::tck::kSmemBytes);
+        rec(5);
     }
-    cudaStream_t ts = both ? aux->tc_stream : st, rs = both ? aux->row_stream : st;
-    cudaStream_t r8s = both ? aux->row8_stream : st;
-    rec(4, ts);
-    if (p.n_items_tc > 0)
-        fa::tck::tc_kernel<<<p.tc_ctas, fa::tck::kThreads, fa::tck::kSmemBytes, ts>>>(p);
-    rec(5, ts);
-    rec(0, r8s);
-    if (p.n_items_r8 > 0)
-        fa::r8k::row8_kernel<<<p.n_items_r8, fa::r8k::kThreads, fa::r8k::kSmemBytes, r8s>>>(p);
-    rec(1, r8s);
-    rec(2, rs);
-    if (p.n_items > 0)
-        fa::rowk::row_kernel<<<p.n_items, fa::rowk::kThreads, fa::rowk::kSmemBytes, rs>>>(p);
-    rec(3, rs);
-    if (both) {
-        if (cudaEventRecord(aux->join_tc, aux->tc_stream) != cudaSuccess ||
-            cudaEventRecord(aux->join_row, aux->row_stream) != cudaSuccess ||
-            cudaEventRecord(aux->join_row8, aux->row8_stream) != cudaSuccess ||
-            cudaStreamWaitEvent(st, aux->join_tc, 0) != cudaSuccess ||
-            cudaStreamWaitEvent(st, aux->join_row, 0) != cudaSuccess ||
-            cudaStreamWaitEvent(st, aux->join_row8, 0) != cudaSuccess)
-            return FA_ERR_CUDA;
-    }
-    rec(6, st);
+    rec(6);
     if (needs_merge(plan)) {
         const int64_t threads = int64_t(p.total_rows) * 32;
         const int blocks = int((threads + fa::mergek::kThreads - 1) / fa::mergek::kThreads);
         fa::mergek::merge_kernel<<<blocks, fa::mergek::kThreads, 0, st>>>(p);
     }
-    rec(7, st);
-    const bool launched = cudaGetLastError() == cudaSuccess;
+    rec(7);
+    const bool launched = ok && cudaGetLastError() == cudaSuccess;
     if (!ev_ok) return FA_ERR_INVALID;
     return launched ? FA_OK : FA_ERR_CUDA;
 }
@@ -253,7 +219,7 @@ extern "C" int fork_attn_plan_upload(fa_plan *plan, void *dev_plan_buf, size_t p
 
 extern "C" int fork_attn_decode_timed(const void *q, const void *k_pages, const void *v_pages,
                                       const fa_plan *plan, void *out, float *lse, void *stream,
-                                      void **events, int32_t n_events, int32_t concurrent) {
+                                      void **events, int32_t n_events) {
     if (!plan || !q || !k_pages || !v_pages || !out || !lse) return FA_ERR_NULL;
     if (!plan->uploaded) return FA_ERR_NOT_UPLOADED;
     if (!aligned(q, 16) || !aligned(k_pages, 16) || !aligned(v_pages, 16) || !aligned(out, 16) ||
@@ -265,12 +231,7 @@ extern "C" int fork_attn_decode_timed(const void *q, const void *k_pages, const 
     fa::DecodeParams p;
     rc = fill_params(plan, q, k_pages, v_pages, out, lse, plan->dev_scratch, p);
     if (rc != FA_OK) return rc;
-    Aux *aux = nullptr;
-    if (concurrent) {
-        aux = aux_for_current_device();
-        if (!aux) return FA_ERR_CUDA;
-    }
-    return launch_all(p, plan, static_cast<cudaStream_t>(stream), events, aux);
+    return launch_all(p, plan, static_cast<cudaStream_t>(stream), events, false);
 }
 
 extern "C" int fork_attn_decode(const void *q, const void *k_pages, const void *v_pages,
@@ -285,9 +246,7 @@ extern "C" int fork_attn_decode(const void *q, const void *k_pages, const void *
     fa::DecodeParams p;
     rc = fill_params(plan, q, k_pages, v_pages, out, lse, plan->dev_scratch, p);
     if (rc != FA_OK) return rc;
-    Aux *aux = aux_for_current_device();
-    if (!aux) return FA_ERR_CUDA;
-    return launch_all(p, plan, static_cast<cudaStream_t>(stream), nullptr, aux);
+    return launch_all(p, plan, static_cast<cudaStream_t>(stream), nullptr, true);
 }
 
 extern "C" int fork_attn_check(fa_plan *plan, int32_t *device_error, void *stream) {
@@ -370,5 +329,5 @@ extern "C" int fork_attn_decode_static_scratch(const void *q, const void *k_page
     p.merge_bases = reinterpret_cast<const int32_t *>(base + L.merge_bases);
     p.mask_words = reinterpret_cast<const uint32_t *>(base + L.mask_words);
     p.err = reinterpret_cast<int32_t *>(base);
-    return launch_all(p, plan, st, nullptr, nullptr);  // one stream: nothing is created here
+    return launch_all(p, plan, st, nullptr, true);  // nothing is created here
 }

@@ -24,6 +24,7 @@
 #include <cmath>
 #include <cstring>
 #include <new>
+#include <queue>
 #include <vector>
 
 #include "plan_internal.h"
@@ -457,20 +458,61 @@ int build_plan(Input &in, const fa_plan_opts &opts, fa_plan *plan) {
     std::stable_sort(em.items_r8.begin(), em.items_r8.end(), by_len);
 
     // Persistent CTAs of the tcgen05 kernel: the SMs it holds while the row kernels stream
-    // the private runs on the others.  Its work is compute (about 1.14 us of one SM per
-    // 128-token tile of one 128-row M tile), theirs is memory (about 130 GB/s per SM they
-    // hold); the split gives each side SMs in proportion to its SM time.  (Both constants are
-    // fitted to B300 sweeps of the split; fa_plan_opts.tensor_ctas > 0 overrides the count.)
+    // the private runs on the others (and on each SM a tcgen05 CTA leaves once the work
+    // counter runs dry).  For every candidate count n the planner replays the device's work
+    // counter -- items in queue order, each to the CTA that frees first -- and lets the row
+    // work stream on the SMs left and freed, then keeps the n whose last kernel ends first.
+    // Rates measured on B300: a tcgen05 item costs about 2.2 us per 128-token tile (one M
+    // tile or two: the per-tile chain is the softmax's) plus 2 us; row work streams about
+    // 85 GB/s per SM beside it and at most 6.2 TB/s in all.  fa_plan_opts.tensor_ctas > 0
+    // overrides the choice.
     {
-        double w_tc = 0.0;
-        for (const fa::Item &it : em.items_tc) {
-            const int T = (em.chunks[it.chunk].n_pages + 7) / 8;
-            w_tc += T * (it.n_rows > fa::kTcRows ? 2.0 : 1.0) * 1.14e-6;
-        }
-        const double w_row = double(st.kv_bytes_rows) / 130e9;
         const int sms = opts.num_sms > 0 ? opts.num_sms : 148;
-        int n = w_tc + w_row > 0.0 ? int(std::lround(sms * w_tc / (w_tc + w_row))) : sms;
-        if (opts.tensor_ctas > 0) n = opts.tensor_ctas;
+        int n_best = std::max<int>(1, std::min<int64_t>(sms, int64_t(em.items_tc.size())));
+        if (!em.items_tc.empty() && st.kv_bytes_rows > 0) {
+            std::vector<double> cost(em.items_tc.size());
+            for (size_t i = 0; i < em.items_tc.size(); ++i)
+                cost[i] = 2.2e-6 * double((em.chunks[em.items_tc[i].chunk].n_pages + 7) / 8) + 2e-6;
+            const double row_bytes = double(st.kv_bytes_rows), rate_sm = 85e9, rate_all = 6.2e12;
+            double t_best = 1e30;
+            std::vector<double> fin;
+            for (int n = 1; n <= std::min<int64_t>(sms, int64_t(em.items_tc.size())); ++n) {
+                // list scheduling in queue order: a min-heap of CTA finish times
+                std::priority_queue<double, std::vector<double>, std::greater<double>> heap;
+                for (int c = 0; c < n; ++c) heap.push(0.0);
+                for (double c : cost) {
+                    const double t = heap.top();
+                    heap.pop();
+                    heap.push(t + c);
+                }
+                fin.clear();
+                while (!heap.empty()) {
+                    fin.push_back(heap.top());
+                    heap.pop();
+                }
+                // row work on the free SMs: sms - n, plus one more at each CTA's finish time
+                double left = row_bytes, t = 0.0;
+                int free_sms = sms - n;
+                for (size_t e = 0; e <= fin.size() && left > 0.0; ++e) {
+                    const double t_next = e < fin.size() ? fin[e] : 1e30;
+                    const double rate = std::min(rate_all, rate_sm * free_sms);
+                    if (rate > 0.0 && left <= rate * (t_next - t)) {
+                        t += left / rate;
+                        left = 0.0;
+                        break;
+                    }
+                    left -= rate * (t_next - t);
+                    t = t_next;
+                    ++free_sms;
+                }
+                const double t_end = std::max(fin.back(), t);
+                if (t_end < t_best * 0.999) {  // the smallest n within 0.1% of the best
+                    t_best = t_end;
+                    n_best = n;
+                }
+            }
+        }
+        int n = opts.tensor_ctas > 0 ? opts.tensor_ctas : n_best;
         n = std::max(1, std::min(n, sms));
         plan->tc_ctas = int32_t(std::min<int64_t>(n, std::max<size_t>(em.items_tc.size(), 1)));
         st.tensor_ctas = em.items_tc.empty() ? 0 : plan->tc_ctas;

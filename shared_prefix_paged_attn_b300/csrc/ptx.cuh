@@ -87,6 +87,11 @@ __device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+// Programmatic dependent launch: this CTA no longer holds back the kernel launched after it
+// with programmatic stream serialization (that kernel may start once every CTA of this grid
+// has executed this or exited).  It orders nothing in memory.
+__device__ __forceinline__ void launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

@@ -12,11 +12,14 @@
 //   O^T += V^T P^T  M = 16 dims (8 tiles of the 128), N = the 8 rows, K = the page's 16
 //                   tokens; P^T is the S^T accumulator turned into a B fragment with two
 //                   movmatrix transposes.
-// Each thread holds 4 scores per page (2 tokens x 2 rows); a row's max is reduced over the
-// 8 lanes sharing its column.  Online softmax in base 2 with a lazy rescale (the running max
-// only moves when it grows by more than 2^8).  Four warps per CTA, each over pages w, w+4, ...
-// with its own 3-stage TMA ring (as the wider row kernel); the warps' (max, sum, O) are
-// combined in shared memory in a fixed order (bitwise run-to-run deterministic).
+// Each thread holds 4 scores per page (2 tokens x 2 rows).  Online softmax in base 2 with a
+// lazy rescale: the running max only moves when a score exceeds it by more than 2^8, which
+// each lane checks on its own scores; only then is the page max of each row reduced over the
+// 8 lanes sharing its column.  Four warps per CTA, each over pages w, w+4, ...
+// with its own 2-stage TMA ring, three CTAs per SM (a warp's page time is mostly its own
+// instruction latency, so more warps per SM stream more than deeper rings); the warps'
+// (max, sum, O) are combined in shared memory in a fixed order (bitwise run-to-run
+// deterministic).
 #pragma once
 #include "decode_params.cuh"
 #include "ptx.cuh"
@@ -27,7 +30,7 @@ namespace r8k {
 constexpr int kRows = 8;
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
-constexpr int kStages = 3;
+constexpr int kStages = 2;  // with 3 CTAs per SM: 12 warps streaming pages per SM
 constexpr int kPageBytes = kPageSize * kHeadDim * 2;  // 4 KiB: one page of one KV head
 constexpr int kSlotBytes = 2 * kPageBytes;             // K then V
 constexpr int kRingBytes = kWarps * kStages * kSlotBytes;
@@ -55,19 +58,20 @@ __device__ __forceinline__ uint32_t swz(uint32_t box, int row, int chunk16) {
 }
 
 __device__ __forceinline__ void issue_page(const DecodeParams &p, uint32_t slot, uint32_t bar, int head, int page) {
+    // one whole-page box each for K and V: [2 halves of 64 dims][16 tokens][128 bytes], the
+    // same image as two 64-dim boxes 2 KiB apart
     ptx::mbar_arrive_expect_tx(bar, kSlotBytes);
-    ptx::tma_load_4d(slot, &p.kmap, bar, 0, 0, head, page);
-    ptx::tma_load_4d(slot + 2048, &p.kmap, bar, 64, 0, head, page);
-    ptx::tma_load_4d(slot + kPageBytes, &p.vmap, bar, 0, 0, head, page);
-    ptx::tma_load_4d(slot + kPageBytes + 2048, &p.vmap, bar, 64, 0, head, page);
+    ptx::tma_load_5d(slot, &p.kmap_page, bar, 0, 0, 0, head, page);
+    ptx::tma_load_5d(slot + kPageBytes, &p.vmap_page, bar, 0, 0, 0, head, page);
 }
 
-__global__ void __launch_bounds__(kThreads, 2) row8_kernel(const __grid_constant__ DecodeParams p) {
+__global__ void __launch_bounds__(kThreads, 3) row8_kernel(const __grid_constant__ DecodeParams p) {
     extern __shared__ uint8_t smem_raw[];
     Smem &sm = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int gid = lane >> 2, tig = lane & 3;
     const Item it = p.items_r8[blockIdx.x];
+    ptx::launch_dependents();  // the next kernel of the decode may take the SMs this grid leaves
     const Chunk ch = p.chunks[it.chunk];
     const int n_pages = ch.n_pages;
     const int32_t *pages = p.chunk_pages + ch.page_off;
@@ -133,10 +137,21 @@ __global__ void __launch_bounds__(kThreads, 2) row8_kernel(const __grid_constant
     bool ok = true;
     const int mi = lane >> 3, r8 = lane & 7;
 
+    // visibility words of this warp's next page for rows ra, rb (all ones: no word), loaded a
+    // page ahead so that their latency hides behind the page before
+    uint32_t wa_nx = 0xFFFFFFFFu, wb_nx = 0xFFFFFFFFu;
+    auto fetch_words = [&](int kq) {
+        if (ra.mask_off >= 0) wa_nx = __ldg(p.mask_words + ra.mask_off + (kq >> 1));
+        if (rb.mask_off >= 0) wb_nx = __ldg(p.mask_words + rb.mask_off + (kq >> 1));
+    };
+    if (need_mask && warp < n_pages) fetch_words(warp);
+
     int j = 0;
     for (;; ++j) {
         const int k = warp + kWarps * j;
         if (k >= n_pages) break;
+        const uint32_t words_a = wa_nx, words_b = wb_nx;
+        if (need_mask && k + kWarps < n_pages) fetch_words(k + kWarps);
         const int s = j % kStages;
         const uint32_t bar = ptx::smem_u32(&sm.bars[warp][s]);
         if (!__all_sync(0xffffffffu, ptx::mbar_wait(bar, (j / kStages) & 1))) {
@@ -146,21 +161,23 @@ __global__ void __launch_bounds__(kThreads, 2) row8_kernel(const __grid_constant
         const uint32_t kb = ring + s * kSlotBytes;
         const uint32_t vb = kb + kPageBytes;
 
-        // ---- S^T = K Q^T: 16 tokens x 8 rows ----
-        float sc[4] = {0.f, 0.f, 0.f, 0.f};
+        // ---- S^T = K Q^T: 16 tokens x 8 rows, even and odd K steps in two independent
+        // accumulator chains (half the dependent MMA latency) ----
+        float sc[4] = {0.f, 0.f, 0.f, 0.f}, sd[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
+        for (int kk = 0; kk < 8; kk += 2) {
             // block mi: tokens r8 + 8 (mi & 1), dims 16 kk + 8 (mi >> 1) .. + 7
-            uint32_t a0, a1, a2, a3;
+            uint32_t a0, a1, a2, a3, c0, c1, c2, c3;
             ptx::ldsm_x4(swz(kb + (kk >> 2) * 2048, r8 + 8 * (mi & 1), 2 * kk + (mi >> 1)), a0, a1, a2, a3);
+            ptx::ldsm_x4(swz(kb + (kk >> 2) * 2048, r8 + 8 * (mi & 1), 2 * kk + 2 + (mi >> 1)), c0, c1, c2, c3);
             ptx::mma_bf16(sc, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
+            ptx::mma_bf16(sd, c0, c1, c2, c3, qb[kk + 1][0], qb[kk + 1][1]);
         }
         // sc: (token gid, row 2 tig), (token gid, row 2 tig + 1), (token gid + 8, ...) x 2
-        float x0 = sc[0] * sl2, x1 = sc[1] * sl2, x2 = sc[2] * sl2, x3 = sc[3] * sl2;
+        float x0 = (sc[0] + sd[0]) * sl2, x1 = (sc[1] + sd[1]) * sl2, x2 = (sc[2] + sd[2]) * sl2,
+              x3 = (sc[3] + sd[3]) * sl2;
         if (need_mask) {
-            uint32_t ka = 0xFFFFu, kb16 = 0xFFFFu;
-            if (ra.mask_off >= 0) ka = (__ldg(p.mask_words + ra.mask_off + (k >> 1)) >> ((k & 1) * 16)) & 0xFFFFu;
-            if (rb.mask_off >= 0) kb16 = (__ldg(p.mask_words + rb.mask_off + (k >> 1)) >> ((k & 1) * 16)) & 0xFFFFu;
+            uint32_t ka = (words_a >> ((k & 1) * 16)) & 0xFFFFu, kb16 = (words_b >> ((k & 1) * 16)) & 0xFFFFu;
             const int lima = ra.climit - 16 * k, limb = rb.climit - 16 * k;
             if (lima < 15) ka &= lima < 0 ? 0u : ((2u << lima) - 1u);
             if (limb < 15) kb16 &= limb < 0 ? 0u : ((2u << limb) - 1u);
@@ -169,17 +186,18 @@ __global__ void __launch_bounds__(kThreads, 2) row8_kernel(const __grid_constant
             if (!((ka >> (gid + 8)) & 1u)) x2 = -INFINITY;
             if (!((kb16 >> (gid + 8)) & 1u)) x3 = -INFINITY;
         }
-        // page max of each row over its 16 tokens (the 8 lanes of this tig)
-        float pa = fmaxf(x0, x2), pb = fmaxf(x1, x3);
+        // The running max only moves when some score of a row exceeds it by more than 2^8
+        // (with ma = -inf any visible score does): each lane checks its own four scores, and
+        // only then are the page maxima reduced over the 8 lanes of each row.
+        const bool grow = x0 > ma + 8.0f || x2 > ma + 8.0f || x1 > mb + 8.0f || x3 > mb + 8.0f;
+        if (__any_sync(0xffffffffu, grow)) {
+            float pa = fmaxf(x0, x2), pb = fmaxf(x1, x3);
 #pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-            pa = fmaxf(pa, __shfl_xor_sync(0xffffffffu, pa, off));
-            pb = fmaxf(pb, __shfl_xor_sync(0xffffffffu, pb, off));
-        }
-        const bool wa = ma == -INFINITY ? pa != -INFINITY : pa > ma + 8.0f;
-        const bool wb = mb == -INFINITY ? pb != -INFINITY : pb > mb + 8.0f;
-        if (__any_sync(0xffffffffu, wa || wb)) {
-            // raise the running max of rows that grew; O^T columns and sums follow
+            for (int off = 4; off < 32; off <<= 1) {
+                pa = fmaxf(pa, __shfl_xor_sync(0xffffffffu, pa, off));
+                pb = fmaxf(pb, __shfl_xor_sync(0xffffffffu, pb, off));
+            }
+            // raise the running max of the rows; O^T columns and sums follow
             const float na = fmaxf(ma, pa), nb = fmaxf(mb, pb);
             const float aa = (ma == -INFINITY || na == -INFINITY) ? 1.f : ptx::ex2(ma - na);
             const float ab = (mb == -INFINITY || nb == -INFINITY) ? 1.f : ptx::ex2(mb - nb);

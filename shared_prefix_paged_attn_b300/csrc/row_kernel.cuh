@@ -61,11 +61,11 @@ __device__ __forceinline__ uint32_t swz(uint32_t box, int row, int chunk16) {
 
 __device__ __forceinline__ void issue_page(const DecodeParams &p, uint32_t slot, uint32_t bar,
                                            int head, int page) {
+    // one whole-page box each for K and V: [2 halves of 64 dims][16 tokens][128 bytes], the
+    // same image as two 64-dim boxes 2 KiB apart
     ptx::mbar_arrive_expect_tx(bar, kSlotBytes);
-    ptx::tma_load_4d(slot, &p.kmap, bar, 0, 0, head, page);
-    ptx::tma_load_4d(slot + 2048, &p.kmap, bar, 64, 0, head, page);
-    ptx::tma_load_4d(slot + kPageBytes, &p.vmap, bar, 0, 0, head, page);
-    ptx::tma_load_4d(slot + kPageBytes + 2048, &p.vmap, bar, 64, 0, head, page);
+    ptx::tma_load_5d(slot, &p.kmap_page, bar, 0, 0, 0, head, page);
+    ptx::tma_load_5d(slot + kPageBytes, &p.vmap_page, bar, 0, 0, 0, head, page);
 }
 
 template <int MT>
@@ -107,10 +107,28 @@ __device__ __forceinline__ void run_pages(const DecodeParams &p, Smem &sm, const
             clim[mt][hr] = ri.climit;
         }
 
+    // visibility words of this warp's next page for its rows (all ones: no word), loaded a page
+    // ahead so that their latency hides behind the page before
+    uint32_t wnx[2][2] = {{0xFFFFFFFFu, 0xFFFFFFFFu}, {0xFFFFFFFFu, 0xFFFFFFFFu}};
+    auto fetch_words = [&](int kq) {
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int hr = 0; hr < 2; ++hr)
+                if (moff[mt][hr] >= 0) wnx[mt][hr] = __ldg(p.mask_words + moff[mt][hr] + (kq >> 1));
+    };
+    if (need_mask && warp < n_pages) fetch_words(warp);
+
     int j = 0;
     for (;; ++j) {
         const int k = warp + kWarps * j;
         if (k >= n_pages) break;
+        uint32_t wcur[2][2];
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+            for (int hr = 0; hr < 2; ++hr) wcur[mt][hr] = wnx[mt][hr];
+        if (need_mask && k + kWarps < n_pages) fetch_words(k + kWarps);
         const int s = j % kStages;
         const uint32_t bar = ptx::smem_u32(&sm.bars[warp][s]);
         const bool landed = __all_sync(0xffffffffu, ptx::mbar_wait(bar, (j / kStages) & 1));
@@ -157,8 +175,7 @@ __device__ __forceinline__ void run_pages(const DecodeParams &p, Smem &sm, const
             for (int hr = 0; hr < 2; ++hr) {
                 uint32_t m16 = 0xFFFFu;
                 if (need_mask) {
-                    if (moff[mt][hr] >= 0)
-                        m16 = (__ldg(p.mask_words + moff[mt][hr] + (k >> 1)) >> ((k & 1) * 16)) & 0xFFFFu;
+                    m16 = (wcur[mt][hr] >> ((k & 1) * 16)) & 0xFFFFu;
                     const int lim = clim[mt][hr] - 16 * k;
                     if (lim < 15) m16 &= (lim < 0) ? 0u : ((2u << lim) - 1u);
                 }
@@ -244,6 +261,7 @@ __global__ void __launch_bounds__(kThreads, 2) row_kernel(const __grid_constant_
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int gid = lane >> 2, tig = lane & 3;
     const Item it = p.items[blockIdx.x];
+    ptx::launch_dependents();  // the next kernel of the decode may take the SMs this grid leaves
     const Chunk ch = p.chunks[it.chunk];
 
     if (tid == 0) {

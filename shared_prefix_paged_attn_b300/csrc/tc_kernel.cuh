@@ -472,6 +472,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
     Smem &sm = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     int32_t *queue = p.err + 1, *done = p.err + 2;
+    ptx::launch_dependents();  // the next kernel of the decode may take the SMs this grid leaves
 
     auto item_ok = [&](int i) {  // items the planner never makes are refused, uniformly
         const Item it = p.items_tc[i];

@@ -192,24 +192,25 @@ def test_tensor_cta_count_does_not_change_results(cfg):
 
 
 def test_timed_decode_matches_decode_bitwise():
+    # the kernels one after another (with events) give the bits of the overlapped decode
     w = W.make(3, small=True)
     dev = torch.device("cuda")
     q, k, v = w.q.to(dev), w.k_pages.to(dev), w.v_pages.to(dev)
     run = fa.ForkAttention(w, out_dtype=fa.FA_F32, tensor_min_rows=16)
     st = run.plan.stats()
     base_out, base_lse = (x.clone() for x in run(q, k, v))
-    for concurrent in (True, False):
-        for _ in range(2):  # twice: the tcgen05 work queue must be reset by the first
-            ev = [torch.cuda.Event(enable_timing=True) for _ in range(8)]
-            run.out.zero_()
-            run.lse.zero_()
-            fa.fork_attn_decode_timed(q, k, v, run.plan, run.out, run.lse, ev,
-                                      concurrent=concurrent)
-            torch.cuda.synchronize()
-            assert fa.fork_attn_check(run.plan) == 0
-            assert torch.equal(run.out, base_out) and torch.equal(run.lse, base_lse)
-            ms = [ev[2 * j].elapsed_time(ev[2 * j + 1]) for j in range(4)]
-            present = [st["num_items_row8"] > 0, st["num_items_rows"] > st["num_items_row8"],
-                       st["num_items_tensor"] > 0, st["merge_rows"] > 0]
-            for t, there in zip(ms, present):
-                assert (t > 0) if there else (0 <= t < 0.005), (ms, present)
+    for _ in range(2):  # twice: the tcgen05 work queue must be reset by the first
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(8)]
+        run.out.zero_()
+        run.lse.zero_()
+        fa.fork_attn_decode_timed(q, k, v, run.plan, run.out, run.lse, ev)
+        torch.cuda.synchronize()
+        assert fa.fork_attn_check(run.plan) == 0
+        assert torch.equal(run.out, base_out) and torch.equal(run.lse, base_lse)
+        ms = [ev[2 * j].elapsed_time(ev[2 * j + 1]) for j in range(4)]
+        present = [st["num_items_row8"] > 0, st["num_items_rows"] > st["num_items_row8"],
+                   st["num_items_tensor"] > 0, st["merge_rows"] > 0]
+        assert all(present)
+        assert all(t > 0 for t in ms), ms
+        out2, lse2 = run(q, k, v)  # and the overlapped decode again after it
+        assert torch.equal(out2, base_out) and torch.equal(lse2, base_lse)
