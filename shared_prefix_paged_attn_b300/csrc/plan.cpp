@@ -275,23 +275,53 @@ int build_plan(Input &in, const fa_plan_opts &opts, fa_plan *plan) {
 
     const fa_desc *s = in.s;
     const int32_t B = s->num_branches, G = in.G, Hkv = in.d->num_kv_heads;
-    const int32_t base_pages = opts.chunk_pages > 0 ? opts.chunk_pages : 64;
     Emit em;
     fa_plan_stats &st = plan->stats;
     std::memset(&st, 0, sizeof st);
 
     const int32_t tmin = opts.tensor_min_rows < 0 ? 0 : (opts.tensor_min_rows > 0 ? opts.tensor_min_rows : 64);
+    auto run_rows = [&](const std::vector<int32_t> &run) {  // stacked rows of a run's readers
+        const int32_t g0 = run[0];
+        int64_t rows = 0;
+        for (int32_t t = 0; t < bd.group_count[g0]; ++t) {
+            const Rec &rd = bd.recs[bd.by_page[bd.group_start[g0] + t]];
+            rows += int64_t(in.q_off[rd.branch + 1] - in.q_off[rd.branch]) * G;
+        }
+        return rows;
+    };
+    // Chunk size of the row kernels' runs: longer chunks mean fewer per-item prologues and
+    // fewer partials to merge, as long as enough items are left to fill every SM with row
+    // CTAs at the end of the decode (one wave: three CTAs on each of 148 SMs).  The largest of
+    // 128, 96, 64 pages that keeps that many row items (measured on B300: the long-context
+    // rolling-drop decode 221 -> 213 us at 128 pages; the flat-fork one, with 256 items at
+    // 64 pages, lost 8% at 128).
+    int32_t base_pages = 64;
+    if (opts.chunk_pages > 0) {
+        base_pages = opts.chunk_pages;
+    } else {
+        const int64_t want = 3 * 148;
+        for (int32_t cand : {128, 96}) {
+            int64_t items = 0;
+            for (const auto &run : runs) {
+                const int64_t rows = run_rows(run);
+                if (tmin > 0 && rows >= tmin) continue;
+                const int64_t target = std::min<int64_t>(std::max<int64_t>(cand, 2 * rows), fa::kMaxChunkPages);
+                items += std::max<int64_t>(1, ceil_div(int64_t(run.size()), target)) *
+                         ceil_div(std::max<int64_t>(rows, 1), fa::kRowsMax) * Hkv;
+            }
+            if (items >= want) {
+                base_pages = cand;
+                break;
+            }
+        }
+    }
     std::vector<char> chunk_tc;  // per chunk: its items go to the tcgen05 kernel
     std::vector<int64_t> chunk_slots;  // per chunk: visible slots of its pages (any reader)
     std::vector<int32_t> occ_count(B, 0);
     for (const auto &run : runs) {
         const int32_t g0 = run[0];
         const int32_t n_read = bd.group_count[g0];
-        int64_t rows = 0;
-        for (int32_t t = 0; t < n_read; ++t) {
-            const Rec &rd = bd.recs[bd.by_page[bd.group_start[g0] + t]];
-            rows += int64_t(in.q_off[rd.branch + 1] - in.q_off[rd.branch]) * G;
-        }
+        const int64_t rows = run_rows(run);
         // fp32 partial rows cost rows * 1 KiB (write + read) per chunk and KV head; a chunk of
         // n pages carries n * 8 KiB of K+V, so n >= 2 * rows keeps partials near 6% of KV.
         int64_t target = std::max<int64_t>(base_pages, 2 * rows);
