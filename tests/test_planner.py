@@ -187,3 +187,25 @@ def test_per_kernel_slot_counters(cfg):
             assert st["tensor_ctas"] == 0
     st = fa.plan_for(w, tensor_min_rows=1, tensor_ctas=3).stats()
     assert st["tensor_ctas"] == min(3, st["num_items_tensor"])
+
+
+def test_row_chunk_length_follows_the_item_count():
+    # long private runs with many row items get chunks of up to 128 pages; the flat-fork
+    # workload, whose 64-page chunks give only 256 row items, keeps them
+    def mean_pages(st):
+        return st["kv_bytes_rows"] / st["num_items_rows"] / (16 * 128 * 2 * 2)
+    long_ctx = fa.plan_for(W.make(4, values=False)).stats()
+    flat = fa.plan_for(W.make(2, values=False)).stats()
+    assert long_ctx["num_items_rows"] >= 3 * 148 and mean_pages(long_ctx) > 64
+    assert flat["num_items_rows"] == 256 and mean_pages(flat) <= 64
+    # an explicit chunk size overrides the choice
+    pinned = fa.plan_for(W.make(4, values=False), chunk_pages=64).stats()
+    assert mean_pages(pinned) <= 64 and pinned["num_items_rows"] > long_ctx["num_items_rows"]
+
+
+def test_tensor_cta_split_matches_the_measured_optima():
+    # the planner's replay of the work counter picks the counts measured best on B300: one
+    # item per CTA for the flat fork's 128 equal items, two per CTA for the 240 items of the
+    # long-context workload (112 CTAs would leave 16 of them a third item)
+    assert fa.plan_for(W.make(2, values=False)).stats()["tensor_ctas"] == 128
+    assert fa.plan_for(W.make(4, values=False)).stats()["tensor_ctas"] == 120
