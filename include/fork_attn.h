@@ -185,8 +185,11 @@ int fork_attn_plan_upload(fa_plan *plan, void *dev_plan_buf, size_t plan_buf_byt
  *   v_pages [device] same layout as k_pages
  *   out     [device] out_dtype [total_q][num_q_heads][128]
  *   lse     [device] fp32 [total_q][num_q_heads]  (natural log)
- * All device pointers must be 16-byte aligned.  Inputs are only read.  Errors: FA_ERR_NULL,
- * FA_ERR_ALIGN, FA_ERR_NOT_UPLOADED, FA_ERR_CUDA (launch failure). */
+ * All device pointers must be 16-byte aligned.  Inputs are only read.  The plan's device
+ * buffers hold the work counters of the persistent tcgen05 kernel and the fp32 partials, so
+ * two decodes of one plan must not overlap on the GPU (one stream, or order them); decodes
+ * of different plans may.  Errors: FA_ERR_NULL, FA_ERR_ALIGN, FA_ERR_NOT_UPLOADED,
+ * FA_ERR_CUDA (launch failure). */
 int fork_attn_decode(const void *q, const void *k_pages, const void *v_pages,
                      const fa_plan *plan, void *out, float *lse, void *stream);
 
