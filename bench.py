@@ -53,12 +53,12 @@ def tensor_peak():
 
 
 def kernel_source_hash():
-    """Short hash of the kernel sources: DRAM traffic read from an ncu capture only counts for the
-    kernels it was taken on."""
+    """Short hash of the decode's sources (planner and kernels; the compaction op is compiled
+    apart): DRAM traffic read from an ncu capture only counts for the kernels it was taken on."""
     import hashlib
     csrc = os.path.join(ROOT, "shared_prefix_paged_attn_b300", "csrc")
     h = hashlib.sha256()
-    for f in sorted(os.listdir(csrc)):
+    for f in sorted(x for x in os.listdir(csrc) if not x.startswith("compact")):
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + b"\0" + fh.read())
     return h.hexdigest()[:12]
@@ -431,6 +431,62 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def run_compact(args):
+    """Physical compaction (with and without repositioning) of the first 8 branches of the
+    workload into fresh pages of a grown pool; one JSON line per mode.  Bytes per launch: the
+    kept entries' K and V read and written (kept x Hkv x 512 B x 2)."""
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    w = W.make(args.config, device=str(dev))
+    branches = list(range(min(8, w.num_branches)))
+    # destination pages for every listed entry (an upper bound on the kept ones)
+    listed = [int(sum(int(w.segs[s][2]) for s in w.branch_segs[w.branch_seg_off[b]:w.branch_seg_off[b + 1]]))
+              for b in branches]
+    need = sum((n + 15) // 16 for n in listed)
+    pool = w.num_pages_pool
+    shape = (pool + need,) + tuple(w.k_pages.shape[1:])
+    k = torch.zeros(shape, dtype=torch.bfloat16, device=dev)
+    v = torch.zeros(shape, dtype=torch.bfloat16, device=dev)
+    k[:pool], v[:pool] = w.k_pages, w.v_pages
+    w.k_pages = w.v_pages = None
+    w.num_pages_pool = shape[0]
+    fresh = np.arange(pool, pool + need, dtype=np.int32)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    hbm_peak, peak_kind = peaks()
+    for rep in (False, True):
+        t0 = time.perf_counter()
+        plan = fa.fork_attn_compact_create(w, branches, fresh, reposition=rep)
+        plan_s = time.perf_counter() - t0
+        kept, wb = plan.sizes()
+        moved = int(kept.sum()) * w.num_kv_heads * KV_BYTES_PER_SLOT_HEAD * 2
+        work = torch.empty(wb // 4 + 64, dtype=torch.int32, device=dev)
+        fa.fork_attn_compact_upload(plan, work)
+        for _ in range(args.warmup):
+            flush.zero_()
+            fa.fork_attn_compact_run(plan, k, v)
+        torch.cuda.synchronize(dev)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        for a, b in ev:
+            flush.zero_()
+            a.record()
+            fa.fork_attn_compact_run(plan, k, v)
+            b.record()
+        torch.cuda.synchronize(dev)
+        ms = sorted(a.elapsed_time(b) for a, b in ev)
+        med = ms[len(ms) // 2]
+        gbs = moved / (med * 1e-3) / 1e9
+        print(json.dumps({"metric": "compaction: kept K/V bytes read + written per second", "op": "compact",
+                          "reposition": rep, "value": gbs, "unit": "GB/s", "ms_per_launch": med,
+                          "ms_min": ms[0], "steps": args.steps, "warmup": args.warmup,
+                          "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+                          "config": {"workload": w.name, "branches": len(branches), "kept_tokens": int(kept.sum()),
+                                     "Hkv": w.num_kv_heads, "bytes_per_launch": moved,
+                                     "l2": "flushed (256 MiB write) between launches", "plan_s": plan_s},
+                          "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
+                                       "frac": gbs / hbm_peak, "peak_kind": peak_kind}}), flush=True)
+        plan.destroy()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -441,10 +497,14 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--compact", action="store_true",
+                    help="time the compaction op (8 branches of --config) instead of the decode")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.impl == "reference":
+    if args.compact:
+        run_compact(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

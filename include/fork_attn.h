@@ -245,6 +245,62 @@ int fork_attn_check(fa_plan *plan, int32_t *device_error, void *stream);
 int fork_attn_decode_static_scratch(const void *q, const void *k_pages, const void *v_pages,
                                     const fa_plan *plan, void *out, float *lse, void *stream);
 
+/* ---- Physical compaction with optional repositioning ----
+ * AgentKV blog (rit.work), "Как AgentKV выбирает и освобождает записи кэша": the kept entries
+ * of a cache are packed into fresh pages, so the freed pages can go back to the allocator and
+ * later decodes read fewer bytes.  AKV (news.farwalk.ai), "AKV 如何工作？": Repos rewrites the
+ * kept keys to positions 0..r-1 with a RoPE rotation, values unchanged.
+ *
+ * For each listed branch, the entries visible in its bits (all of them without bits) are
+ * copied in logical order to destination pages: the n-th kept entry of the branch to slot
+ * n % page_size of the branch's (n / page_size)-th destination page.  V is copied as is; K too
+ * unless reposition != 0, in which case the key of the entry at logical index j is rotated
+ * by the position change d = n - j: for i < head_dim / 2 with theta_i =
+ * rope_base^(-2 i / head_dim), the pair (x_i, x_{i + head_dim/2}) becomes
+ * (x_i cos(d theta_i) - x_{i+h} sin(d theta_i), x_{i+h} cos(d theta_i) + x_i sin(d theta_i))
+ * (rotate-half pairing), computed in fp32 and rounded to bf16 (nearest even). */
+typedef struct {
+    int32_t num_kv_heads;
+    int32_t head_dim;     /* 128 */
+    int32_t page_size;    /* 16 */
+    int32_t reposition;   /* 0: keys copied; 1: keys rotated from position j to n (Repos) */
+    double rope_base;     /* > 1; used when reposition != 0 */
+} fa_compact_dims;
+
+typedef struct fa_compact fa_compact; /* opaque; owned by the library */
+
+/* Plans the compaction of branches[0 .. num_branches) of `desc` (host arrays, read here
+ * only).  Destination pages are dst_page_ids [host], consumed branch after branch, each branch
+ * from a fresh page (ceil(r / page_size) pages for r kept entries).  They must not be pages of
+ * any listed branch (the gather runs in place in the same pool) and must not hold anything
+ * another reader still needs.  Errors: FA_ERR_NULL, FA_ERR_INVALID (branch index, bad CSR or
+ * segment, too few destination pages, a destination page listed twice or read by a listed
+ * branch, rope_base <= 1 with reposition), FA_ERR_RANGE (page id, segment id or bit word out
+ * of range; a pool of more than 2^27 pages), FA_ERR_UNSUPPORTED (head_dim != 128, page_size
+ * != 16), FA_ERR_NOMEM.  *out is set only on FA_OK. */
+int fork_attn_compact_create(const fa_compact_dims *dims, const fa_desc *desc,
+                             const int32_t *branches, int32_t num_branches,
+                             const int32_t *dst_page_ids, int64_t num_dst_pages,
+                             fa_compact **out);
+
+/* kept_tokens [host, num_branches] (may be NULL): r per listed branch.  work_bytes (may be
+ * NULL): the size of the device work buffer of fork_attn_compact_upload. */
+int fork_attn_compact_sizes(const fa_compact *c, int64_t *kept_tokens, size_t *work_bytes);
+
+/* Copies the plan's slot lists into dev_work [device, 256-byte aligned, >= work_bytes] on
+ * `stream` (from the plan's host memory: keep the plan until the stream has passed the copy).
+ * Errors: FA_ERR_NULL, FA_ERR_ALIGN, FA_ERR_BUFFER_SMALL, FA_ERR_CUDA. */
+int fork_attn_compact_upload(fa_compact *c, void *dev_work, size_t work_bytes, void *stream);
+
+/* Runs the gather on `stream`: k_pages, v_pages [device, 16-byte aligned] bf16
+ * [num_pages_pool][num_kv_heads][16][128] are read at the kept slots and written at the
+ * destination slots.  No allocation, no host synchronisation; running it again rewrites the
+ * same destinations.  Errors: FA_ERR_NULL, FA_ERR_ALIGN, FA_ERR_NOT_UPLOADED, FA_ERR_CUDA. */
+int fork_attn_compact_run(const fa_compact *c, void *k_pages, void *v_pages, void *stream);
+
+/* Frees the compaction plan (not the caller's device buffers). */
+int fork_attn_compact_destroy(fa_compact *c);
+
 /* Frees the host plan.  Device buffers stay owned by the caller. */
 int fork_attn_plan_destroy(fa_plan *plan);
 

@@ -11,11 +11,11 @@ from typing import Optional
 import numpy as np
 
 from . import _lib
-from ._lib import FA_BF16, FA_F32, FaDesc, FaDims, FaPlanOpts, FaPlanStats
+from ._lib import FA_BF16, FA_F32, FaCompactDims, FaDesc, FaDims, FaPlanOpts, FaPlanStats
 
 __all__ = ["ForkAttnError", "Plan", "fork_attn_plan_create", "fork_attn_decode",
            "fork_attn_decode_timed", "fork_attn_decode_static_scratch", "fork_attn_check", "fork_attn_strerror", "FA_BF16",
-           "FA_F32", "plan_for", "ForkAttention"]
+           "FA_F32", "plan_for", "ForkAttention", "CompactPlan", "fork_attn_compact_create", "fork_attn_compact_upload", "fork_attn_compact_run"]
 
 
 class ForkAttnError(RuntimeError):
@@ -83,6 +83,25 @@ class Plan:
             pass
 
 
+def _desc(arr, page_ids, segs, branch_seg_off, branch_segs, num_pages_pool, branch_q_off,
+          vis_bits, vis_word_off) -> FaDesc:
+    segs = np.ascontiguousarray(segs, dtype=np.int32).reshape(-1, 3)
+    desc = FaDesc()
+    desc.page_ids = arr(page_ids, np.int32)
+    desc.num_page_ids = len(page_ids)
+    desc.segs = arr(segs, np.int32)
+    desc.num_segs = len(segs)
+    desc.branch_seg_off = arr(branch_seg_off, np.int32)
+    desc.branch_segs = arr(branch_segs, np.int32)
+    desc.num_branches = len(branch_seg_off) - 1
+    desc.branch_q_off = arr(branch_q_off, np.int32)
+    desc.vis_bits = arr(vis_bits, np.uint32)
+    desc.vis_word_off = arr(vis_word_off, np.int64)
+    desc.num_vis_words = 0 if vis_bits is None else len(vis_bits)
+    desc.num_pages_pool = int(num_pages_pool)
+    return desc
+
+
 def fork_attn_plan_create(num_q_heads, num_kv_heads, page_ids, segs, branch_seg_off,
                           branch_segs, num_pages_pool, branch_q_off=None, vis_bits=None,
                           vis_word_off=None, scale=None, out_dtype=FA_BF16, head_dim=128,
@@ -100,20 +119,8 @@ def fork_attn_plan_create(num_q_heads, num_kv_heads, page_ids, segs, branch_seg_
 
     dims = FaDims(int(num_q_heads), int(num_kv_heads), int(head_dim), int(page_size),
                   float(scale if scale is not None else 1.0 / np.sqrt(head_dim)), int(out_dtype))
-    segs = np.ascontiguousarray(segs, dtype=np.int32).reshape(-1, 3)
-    desc = FaDesc()
-    desc.page_ids = arr(page_ids, np.int32)
-    desc.num_page_ids = len(page_ids)
-    desc.segs = arr(segs, np.int32)
-    desc.num_segs = len(segs)
-    desc.branch_seg_off = arr(branch_seg_off, np.int32)
-    desc.branch_segs = arr(branch_segs, np.int32)
-    desc.num_branches = len(branch_seg_off) - 1
-    desc.branch_q_off = arr(branch_q_off, np.int32)
-    desc.vis_bits = arr(vis_bits, np.uint32)
-    desc.vis_word_off = arr(vis_word_off, np.int64)
-    desc.num_vis_words = 0 if vis_bits is None else len(vis_bits)
-    desc.num_pages_pool = int(num_pages_pool)
+    desc = _desc(arr, page_ids, segs, branch_seg_off, branch_segs, num_pages_pool, branch_q_off,
+                 vis_bits, vis_word_off)
     opts = FaPlanOpts()
     opts.chunk_pages, opts.num_sms, opts.tensor_min_rows = int(chunk_pages), int(num_sms), int(tensor_min_rows)
     opts.tensor_ctas, opts.tensor_chunk_pages = int(tensor_ctas), int(tensor_chunk_pages)
@@ -189,3 +196,67 @@ class ForkAttention:
     def __call__(self, q, k_pages, v_pages, stream=None):
         fork_attn_decode(q, k_pages, v_pages, self.plan, self.out, self.lse, stream)
         return self.out, self.lse
+
+
+class CompactPlan:
+    """Host handle of a compaction plan (fork_attn_compact_*); freed on destroy() or GC."""
+
+    def __init__(self, handle: int, keep, n_branches: int):
+        self.handle = handle
+        self._keep = keep
+        self.n_branches = n_branches
+
+    def sizes(self):
+        kept = np.zeros(self.n_branches, dtype=np.int64)
+        wb = ctypes.c_size_t()
+        _check(_lib.load().fork_attn_compact_sizes(self.handle, kept.ctypes.data, ctypes.byref(wb)),
+               "fork_attn_compact_sizes")
+        return kept, wb.value
+
+    def destroy(self):
+        if self.handle:
+            _lib.load().fork_attn_compact_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.destroy()
+        except Exception:
+            pass
+
+
+def fork_attn_compact_create(w, branches, dst_page_ids, reposition=False, rope_base=10000.0,
+                             head_dim=128, page_size=16) -> CompactPlan:
+    """fork_attn_compact_create for a ``workloads.Workload``-like descriptor (host arrays)."""
+    keep = []
+
+    def arr(x, dt):
+        if x is None:
+            return None
+        a = np.ascontiguousarray(x, dtype=dt)
+        keep.append(a)
+        return a.ctypes.data
+
+    desc = _desc(arr, w.page_ids, w.segs, w.branch_seg_off, w.branch_segs, w.num_pages_pool,
+                 w.branch_q_off, w.vis_bits, w.vis_word_off)
+    dims = FaCompactDims(int(w.num_kv_heads), int(head_dim), int(page_size), int(bool(reposition)),
+                         float(rope_base))
+    br = np.ascontiguousarray(branches, dtype=np.int32)
+    dst = np.ascontiguousarray(dst_page_ids, dtype=np.int32)
+    keep += [br, dst, desc, dims]
+    handle = ctypes.c_void_p()
+    _check(_lib.load().fork_attn_compact_create(ctypes.byref(dims), ctypes.byref(desc), br.ctypes.data,
+                                                len(br), dst.ctypes.data, len(dst), ctypes.byref(handle)),
+           "fork_attn_compact_create")
+    return CompactPlan(handle.value, keep, len(br))
+
+
+def fork_attn_compact_upload(plan: CompactPlan, work, stream=None):
+    _check(_lib.load().fork_attn_compact_upload(plan.handle, _ptr(work), work.numel() * work.element_size(),
+                                                _stream_ptr(stream)), "fork_attn_compact_upload")
+    plan._work = work  # the device buffer must outlive the plan's runs
+
+
+def fork_attn_compact_run(plan: CompactPlan, k_pages, v_pages, stream=None):
+    _check(_lib.load().fork_attn_compact_run(plan.handle, _ptr(k_pages), _ptr(v_pages), _stream_ptr(stream)),
+           "fork_attn_compact_run")

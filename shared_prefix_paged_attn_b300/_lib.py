@@ -49,6 +49,11 @@ class FaPlanStats(ctypes.Structure):
                 ("unique_slots_row32", c_int64), ("tensor_ctas", c_int64)]
 
 
+class FaCompactDims(ctypes.Structure):
+    _fields_ = [("num_kv_heads", c_int32), ("head_dim", c_int32), ("page_size", c_int32),
+                ("reposition", c_int32), ("rope_base", ctypes.c_double)]
+
+
 # name -> (restype, argtypes); every symbol declared in include/fork_attn.h
 SIGNATURES = {
     "fork_attn_plan_create": (c_int32, [ctypes.POINTER(FaDims), ctypes.POINTER(FaDesc),
@@ -66,6 +71,13 @@ SIGNATURES = {
     "fork_attn_decode_static_scratch": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p,
                                                   c_void_p, c_void_p, c_void_p]),
     "fork_attn_plan_destroy": (c_int32, [c_void_p]),
+    "fork_attn_compact_create": (c_int32, [ctypes.POINTER(FaCompactDims), ctypes.POINTER(FaDesc),
+                                           c_void_p, c_int32, c_void_p, ctypes.c_int64,
+                                           ctypes.POINTER(c_void_p)]),
+    "fork_attn_compact_sizes": (c_int32, [c_void_p, c_void_p, ctypes.POINTER(ctypes.c_size_t)]),
+    "fork_attn_compact_upload": (c_int32, [c_void_p, c_void_p, ctypes.c_size_t, c_void_p]),
+    "fork_attn_compact_run": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p]),
+    "fork_attn_compact_destroy": (c_int32, [c_void_p]),
     "fork_attn_strerror": (ctypes.c_char_p, [c_int32]),
 }
 
