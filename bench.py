@@ -52,15 +52,26 @@ def tensor_peak():
     return FALLBACK_BF16_TFLOPS, "fallback"
 
 
-def kernel_source_hash():
-    """Short hash of the decode's sources (planner and kernels; the compaction op is compiled
-    apart): DRAM traffic read from an ncu capture only counts for the kernels it was taken on."""
+def code_text(src: str) -> str:
+    """C/C++/CUDA source with each comment and each run of whitespace turned into one space
+    (string and character literals kept), so that a comment or layout edit leaves the hash of
+    the code unchanged."""
+    import re
+    tok = re.compile(r'//[^\n]*|/\*.*?\*/|"(?:\\.|[^"\\])*"|\'(?:\\.|[^\'\\])*\'|\s+', re.S)
+    out = tok.sub(lambda m: m.group(0) if m.group(0)[0] in "\"'" else "\0", src)
+    return re.sub("\0+", " ", out).strip()
+
+
+def kernel_source_hash(read=None):
+    """Short hash of the decode's code (planner and kernels, comments and whitespace removed;
+    the compaction op is compiled apart): DRAM traffic read from an ncu capture only counts
+    for the kernels it was taken on."""
     import hashlib
     csrc = os.path.join(ROOT, "shared_prefix_paged_attn_b300", "csrc")
+    read = read or (lambda f: open(os.path.join(csrc, f), encoding="utf-8").read())
     h = hashlib.sha256()
     for f in sorted(x for x in os.listdir(csrc) if not x.startswith("compact")):
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(f.encode() + b"\0" + fh.read())
+        h.update(f.encode() + b"\0" + code_text(read(f)).encode())
     return h.hexdigest()[:12]
 
 

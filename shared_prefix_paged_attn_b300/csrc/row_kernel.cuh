@@ -7,9 +7,10 @@
 //
 // Design (sm_103a):
 //   - one CTA = 4 warps per work item (chunk x KV head x row group); warp w owns pages
-//     w, w+4, w+8, ... of the chunk and runs its own 3-stage ring: lane 0 issues four 2 KiB
-//     TMA tensor loads per page (K and V, two 64-dim halves each, 128-byte swizzle) that
-//     complete on the slot's mbarrier;
+//     w, w+4, w+8, ... of the chunk and runs its own 3-stage ring: lane 0 issues two TMA
+//     tensor loads per page (K and V, each a whole page-head of two 64-dim halves, 128-byte
+//     swizzle) that complete on the slot's mbarrier; the rows' visibility words are loaded a
+//     page ahead;
 //   - the dot products run on the warp MMA (m16n8k16 bf16 -> fp32): S = Q K^T with the
 //     stacked rows as M (one or two 16-row tiles), then O += P V with P taken from the S
 //     accumulators without leaving registers;
