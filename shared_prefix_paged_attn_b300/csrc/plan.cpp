@@ -17,9 +17,13 @@
 //      lie before every reader's query tokens, when the same readers read p' further on;
 //      pages that no reader sees at all are skipped;
 //   5. cut runs into chunks (long enough that fp32 partial results stay a few percent of the
-//      KV bytes, short enough for occupancy), pack per-reader visibility words, give every
-//      (chunk, reader) its partial rows (or a direct write when it is the branch's only one);
-//   6. emit work items = chunk x KV head x row group and the per-branch merge lists.
+//      KV bytes, short enough for occupancy: up to 128 pages for the row kernels while a full
+//      wave of row items remains, whole 8-page tiles for the tcgen05 kernel), pack per-reader
+//      visibility words, give every (chunk, reader) its partial rows (or a direct write when
+//      it is the branch's only one);
+//   6. emit work items = chunk x KV head x row group and the per-branch merge lists;
+//   7. choose the tcgen05 kernel's persistent CTA count by replaying its work counter beside
+//      the row work streaming on the SMs left and freed.
 #include <algorithm>
 #include <cmath>
 #include <cstring>

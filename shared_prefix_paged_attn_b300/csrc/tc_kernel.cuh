@@ -8,7 +8,10 @@
 // (branch, query token, query head of the KV head's GQA group) reading the chunk is one row
 // of Q, so S = Q K^T and O += P V are dense M = 128 contractions on tcgen05.
 //
-// One CTA = 12 warps per work item (chunk x KV head x row group of <= 256 rows):
+// Persistent: the planner's number of CTAs (one per SM, the others left to the row kernels)
+// take work items (chunk x KV head x row group of <= 256 rows) from a counter in the plan
+// buffer; each CTA of 12 warps runs its items one after another, keeping its TMEM and
+// re-initialising its mbarriers in between.  Per item:
 //   warps 0 and 2        TMA producers: per 128-token tile, warp 0 loads the 8 pages of K as
 //                        2 KiB boxes (64 dims x 16 tokens, 128-byte swizzle) into a 2-stage
 //                        K ring, warp 2 the 8 pages of V as whole 4 KiB page boxes into a
