@@ -209,3 +209,24 @@ def test_tensor_cta_split_matches_the_measured_optima():
     # long-context workload (112 CTAs would leave 16 of them a third item)
     assert fa.plan_for(W.make(2, values=False)).stats()["tensor_ctas"] == 128
     assert fa.plan_for(W.make(4, values=False)).stats()["tensor_ctas"] == 120
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_prefill_shaped_descriptors_plan_like_decodes(seed):
+    # every token a query (n_q = n_b): the packed-prefill case of the same definition; the
+    # planner accepts it and its counters keep their meaning
+    w = W.random_dag(900 + seed, n_branches=3, n_segs=3, max_seg_len=60, pool_pages=30,
+                     drop_p=0.2, values=False)
+    lens = [w.branch_len(b) for b in range(w.num_branches)]
+    w.branch_q_off = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    st = fa.plan_for(w).stats()
+    assert st["total_q"] == sum(lens)
+    assert (st["unique_visible_slots"], st["touched_pages"]) == oracle.unique_slots(w)
+    G = w.num_q_heads // w.num_kv_heads
+    want = sum(_visible_positions(w, b) * lens[b] for b in range(w.num_branches)) * G * w.num_kv_heads * 4 * 128
+    assert st["flops_rows"] + st["flops_tensor"] == want
+    # one token too many is refused
+    w.branch_q_off = w.branch_q_off.copy()
+    w.branch_q_off[1:] += 1
+    with pytest.raises(fa.ForkAttnError):
+        fa.plan_for(w)
