@@ -94,91 +94,101 @@ def ncu_traffic(workload):
 
 
 class ClockSampler:
-    """Samples SM clock and throttle reasons through NVML while the timed region runs."""
+    """Samples the SM clock and the throttle reasons while a timed region runs.
 
-    def __init__(self, index, period_s=0.02):
+    One sample is taken synchronously on entry and one on exit (right before and right after
+    the region: a short region still yields a record), and a thread samples every `period_s`
+    in between.  NVML through ``pynvml`` when it loads, else one-shot ``nvidia-smi`` queries."""
+
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+    def __init__(self, index, period_s=0.002):
         self.index, self.period = index, period_s
         self.samples, self.reasons = [], set()
         self.max_mhz = None
         self._stop = threading.Event()
         self._thr = None
+        self._h = None
+        self.source = None
 
-    def __enter__(self):
+    def _bits(self):
+        import pynvml
+        return {
+            "hw_slowdown": getattr(pynvml, "nvmlClocksEventReasonHwSlowdown", 0x8),
+            "hw_thermal_slowdown": getattr(pynvml, "nvmlClocksEventReasonHwThermalSlowdown", 0x40),
+            "sw_thermal_slowdown": getattr(pynvml, "nvmlClocksEventReasonSwThermalSlowdown", 0x20),
+            "sw_power_cap": getattr(pynvml, "nvmlClocksEventReasonSwPowerCap", 0x4),
+            "hw_power_brake_slowdown": getattr(pynvml, "nvmlClocksEventReasonHwPowerBrakeSlowdown", 0x80),
+        }
+
+    def _sample_nvml(self):
+        import pynvml
         try:
-            import pynvml
-            pynvml.nvmlInit()
-            h = pynvml.nvmlDeviceGetHandleByIndex(self.index)
-            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(h, pynvml.NVML_CLOCK_SM)
-            names = {
-                "hw_slowdown": getattr(pynvml, "nvmlClocksEventReasonHwSlowdown", 0x8),
-                "hw_thermal_slowdown": getattr(pynvml, "nvmlClocksEventReasonHwThermalSlowdown", 0x40),
-                "sw_thermal_slowdown": getattr(pynvml, "nvmlClocksEventReasonSwThermalSlowdown", 0x20),
-                "sw_power_cap": getattr(pynvml, "nvmlClocksEventReasonSwPowerCap", 0x4),
-                "hw_power_brake_slowdown": getattr(pynvml, "nvmlClocksEventReasonHwPowerBrakeSlowdown", 0x80),
-            }
+            self.samples.append(float(pynvml.nvmlDeviceGetClockInfo(self._h, pynvml.NVML_CLOCK_SM)))
+            fn = getattr(pynvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                pynvml.nvmlDeviceGetCurrentClocksThrottleReasons
+            r = fn(self._h)
+            for n, bit in self._bits().items():
+                if r & bit:
+                    self.reasons.add(n)
+        except Exception as e:  # keep sampling; record that a query failed
+            self.reasons.add(f"query_failed:{type(e).__name__}")
 
-            def loop():
-                while not self._stop.is_set():
-                    try:
-                        self.samples.append(pynvml.nvmlDeviceGetClockInfo(h, pynvml.NVML_CLOCK_SM))
-                        r = pynvml.nvmlDeviceGetCurrentClocksEventReasons(h)
-                        for n, bit in names.items():
-                            if r & bit:
-                                self.reasons.add(n)
-                    except Exception:
-                        pass
-                    time.sleep(self.period)
-
-            self._thr = threading.Thread(target=loop, daemon=True)
-            self._thr.start()
-        except Exception as e:  # no NVML binding: sample nvidia-smi instead
-            self.nvml_error = f"{type(e).__name__}: {e}"
-            self._start_smi()
-        return self
-
-    def _start_smi(self):
+    def _sample_smi(self):
         import subprocess
-        q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
-             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
-             "clocks_event_reasons.sw_power_cap")
+        q = "clocks.sm,clocks.max.sm," + ",".join("clocks_event_reasons." + n for n in self.NAMES)
         try:
-            self._smi = subprocess.Popen(
-                ["nvidia-smi", f"--query-gpu={q}", "-i", str(self.index),
-                 "--format=csv,noheader,nounits", "-lms", "20"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            out = subprocess.run(["nvidia-smi", f"--query-gpu={q}", "-i", str(self.index),
+                                  "--format=csv,noheader,nounits"], capture_output=True,
+                                 text=True, timeout=20).stdout
         except Exception as e:
             self.reasons.add(f"clock_sampling_unavailable:{type(e).__name__}")
-            self._smi = None
-
-    def _stop_smi(self):
-        if getattr(self, "_smi", None) is None:
             return
-        self._smi.terminate()
-        out, _ = self._smi.communicate(timeout=10)
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in out.splitlines():
             f = [x.strip() for x in line.split(",")]
-            if len(f) < 6:
+            if len(f) < 2 + len(self.NAMES):
                 continue
             try:
                 self.samples.append(float(f[0]))
                 self.max_mhz = float(f[1])
             except ValueError:
                 continue
-            for n, v in zip(names, f[2:6]):
+            for n, v in zip(self.NAMES, f[2:]):
                 if v.lower() in ("active", "1", "yes"):
                     self.reasons.add(n)
 
+    def __enter__(self):
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self._h = pynvml.nvmlDeviceGetHandleByIndex(self.index)
+            self.max_mhz = float(pynvml.nvmlDeviceGetMaxClockInfo(self._h, pynvml.NVML_CLOCK_SM))
+            self.source = "nvml"
+        except Exception as e:
+            self.nvml_error = f"{type(e).__name__}: {e}"
+            self.source = "nvidia-smi"
+        sample = self._sample_nvml if self.source == "nvml" else self._sample_smi
+        sample()  # right before the region
+
+        def loop():
+            while True:  # sample first, then look at the stop flag
+                sample()
+                if self._stop.wait(self.period if self.source == "nvml" else 0.05):
+                    break
+
+        self._thr = threading.Thread(target=loop, daemon=True)
+        self._thr.start()
+        return self
+
     def __exit__(self, *a):
         self._stop.set()
-        if self._thr:
-            self._thr.join()
-        self._stop_smi()
+        self._thr.join()
+        (self._sample_nvml if self.source == "nvml" else self._sample_smi)()  # right after
 
     def record(self):
         return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
                 "sm_max_mhz": self.max_mhz, "samples": len(self.samples),
-                "reasons": sorted(self.reasons)}
+                "reasons": sorted(self.reasons), "source": self.source}
 
 
 def dist_setup(n_gpus):
@@ -239,6 +249,14 @@ def host_copy(w):
     return (w.q.cpu().pin_memory(), w.k_pages.cpu().pin_memory(), w.v_pages.cpu().pin_memory())
 
 
+def workload_config(w, unique_bytes):
+    """The `config` dict of a bench line: the same keys and values in both arms."""
+    return {"workload": w.name, "config_id": int(w.meta.get("config_id", 0)),
+            "Hq": w.num_q_heads, "Hkv": w.num_kv_heads, "branches": w.num_branches,
+            "total_q": w.total_q, "unique_kv_bytes": int(unique_bytes),
+            "l2": "flushed (256 MiB write) between steps"}
+
+
 def run_reference(args):
     """The oracle as it stands, on the host cores: one (branch, KV head) task per step."""
     dist, rank, world, local = dist_setup(args.gpus)
@@ -247,6 +265,7 @@ def run_reference(args):
     import oracle
     dev = "cuda" if torch.cuda.is_available() else "cpu"  # torch's RNG only draws the inputs
     w = W.make(args.config, device=dev)
+    w.meta["config_id"] = args.config
     w.q, w.k_pages, w.v_pages = w.q.cpu(), w.k_pages.cpu(), w.v_pages.cpu()
     unique_bytes = oracle.unique_slots(w)[0] * w.num_kv_heads * KV_BYTES_PER_SLOT_HEAD
     Hq, Hkv = w.num_q_heads, w.num_kv_heads
@@ -267,7 +286,7 @@ def run_reference(args):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "config_id": args.config},
+            "config": workload_config(w, unique_bytes),
             "cpu_baseline": {"value": value, "unit": "GB/s", "cores": oracle.threads_default(),
                              "kind": "oracle",
                              "sample": "per step one (branch, KV head) of the workload, fp64 "
@@ -277,18 +296,51 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
-def run_ours(args):
-    dist, rank, world, local = dist_setup(args.gpus)
-    dev = torch.device("cuda", local if world > 1 else 0)
-    torch.cuda.set_device(dev)
-    w = rank_workload(args.config, rank, str(dev))
+KERNEL_NAMES = ["row8_kernel", "row_kernel", "tcgen05_kernel", "merge_kernel"]
+
+
+def kernels_present(st):
+    return [st["num_items_row8"] > 0, st["num_items_rows"] > st["num_items_row8"],
+            st["num_items_tensor"] > 0, st["merge_rows"] > 0]
+
+
+def kernel_rooflines(st, w, avg, traffic):
+    """Per-kernel roofline entries from the one-by-one timings `avg` (ms, KERNEL_NAMES order)."""
+    hbm_peak, peak_kind = peaks()
+    tflops_peak, tpeak_kind = tensor_peak()
+    part_bytes = st["partial_rows"] * (128 * 4 + 4) * 2  # fp32 partial O + lse, written then read
+    slots = {"row8_kernel": st["unique_slots_row8"], "row_kernel": st["unique_slots_row32"]}
+    kernels = {}
+    for j, n in enumerate(KERNEL_NAMES):
+        if not kernels_present(st)[j]:
+            continue
+        if n == "tcgen05_kernel":
+            alg, unit, peak, pk, bound = st["flops_tensor"], "TFLOP/s", tflops_peak, tpeak_kind, "tensor"
+            scale = 1e12
+        else:
+            alg = (slots[n] * w.num_kv_heads * KV_BYTES_PER_SLOT_HEAD if n in slots
+                   else part_bytes // 2 + st["merge_rows"] * (128 * 2 + 4))
+            unit, peak, pk, bound, scale = "GB/s", hbm_peak, peak_kind, "hbm", 1e9
+        ach = alg / (avg[j] * 1e-3) / scale
+        kernels[n] = {"bound": bound, "achieved": ach, "peak": peak, "unit": unit,
+                      "frac": ach / peak, "ms": avg[j], "peak_kind": pk, "algorithmic": alg,
+                      "traffic": traffic.get(n)}
+    return kernels
+
+
+def measure_config(cfg, args, dev, flush, dist, rank, world, steps, keep=False):
+    """Plans one workload, runs `steps` timed decodes (L2 flushed before each, CUDA events on
+    the launching stream, clocks sampled) and then the same number of one-by-one decodes for
+    the per-kernel times.  Returns a dict; with keep=True it also holds the workload and the
+    ForkAttention object (for the end-to-end and CPU legs)."""
+    w = rank_workload(cfg, rank, str(dev))
+    w.meta["config_id"] = cfg
     t0 = time.perf_counter()
     run = fa.ForkAttention(w, out_dtype=fa.FA_BF16, device=dev)
     plan_s = time.perf_counter() - t0
     st = run.plan.stats()
     unique_bytes = st["unique_visible_slots"] * w.num_kv_heads * KV_BYTES_PER_SLOT_HEAD
     stream = torch.cuda.current_stream(dev)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     q, k, v = w.q, w.k_pages, w.v_pages
 
     def step(events=None):
@@ -303,17 +355,15 @@ def run_ours(args):
     torch.cuda.synchronize(dev)
     assert fa.fork_attn_check(run.plan, stream) == 0, "device error word set during warm-up"
 
-    # The timed region: K steps of fork_attn_decode exactly as a caller runs it.
-    K = args.steps
-    names = ["row8_kernel", "row_kernel", "tcgen05_kernel", "merge_kernel"]
-    ev_start = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    ev_stop = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    # The timed region: `steps` decodes exactly as a caller runs them.
+    ev_start = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ev_stop = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     if dist:
         dist.barrier()
     torch.cuda.synchronize(dev)
     wall0 = time.perf_counter()
     with ClockSampler(dev.index if dev.index is not None else 0) as clk:
-        for i in range(K):
+        for i in range(steps):
             flush.zero_()
             ev_start[i].record(stream)
             step()
@@ -324,48 +374,50 @@ def run_ours(args):
         dist.barrier()
     step_ms = [a.elapsed_time(b) for a, b in zip(ev_start, ev_stop)]
     assert fa.fork_attn_check(run.plan, stream) == 0, "device error word set in the timed region"
-    ms = sum(step_ms) / K
+    ms = sum(step_ms) / steps
     ms_max = max_over_ranks(dist, ms, dev)
-    value = unique_bytes * world / (ms_max * 1e-3) / 1e9
-    bq_s = w.total_q * world / (ms_max * 1e-3)
 
     # Per-kernel durations: inside the decode the kernels overlap on one stream (the row
     # kernels are programmatic dependent launches beside the tcgen05 kernel), where a CUDA
     # event between two of them would serialise them.  So each kernel is timed alone, with
-    # CUDA events on the launching stream, in Kk further steps of the same decode with its
+    # CUDA events on the launching stream, in further steps of the same decode with its
     # kernels one after another (fork_attn_decode_timed), L2 flushed before every step.
-    Kk = min(K, 100)
-    aev = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * len(names))] for _ in range(Kk)]
+    Kk = min(steps, 100)
+    aev = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * len(KERNEL_NAMES))] for _ in range(Kk)]
     for i in range(Kk):
         flush.zero_()
         step(aev[i])
     torch.cuda.synchronize(dev)
     assert fa.fork_attn_check(run.plan, stream) == 0, "device error word set in the one-by-one pass"
     avg = [sum(aev[i][2 * j].elapsed_time(aev[i][2 * j + 1]) for i in range(Kk)) / Kk
-           for j in range(len(names))]
+           for j in range(len(KERNEL_NAMES))]
+    kernels = kernel_rooflines(st, w, avg, ncu_traffic(w.name))
+    hbm_peak, _ = peaks()
+    value = unique_bytes * world / (ms_max * 1e-3) / 1e9
+    res = {"cfg": cfg, "w": w if keep else None, "run": run if keep else None, "stats": st,
+           "unique_bytes": unique_bytes, "plan_s": plan_s, "ms": ms_max, "step_ms": step_ms,
+           "wall": wall, "value": value, "bq_s": w.total_q * world / (ms_max * 1e-3),
+           "frac": value / world / hbm_peak, "kernels": kernels,
+           "kernel_ms": {n: a for n, a, p in zip(KERNEL_NAMES, avg, kernels_present(st)) if p},
+           "clocks": clk.record(), "config": workload_config(w, unique_bytes), "Kk": Kk,
+           "launches_per_step": sum(kernels_present(st))}
+    if not keep:
+        del run, w, q, k, v
+        torch.cuda.empty_cache()
+    return res
 
-    hbm_peak, peak_kind = peaks()
-    tflops_peak, tpeak_kind = tensor_peak()
-    traffic = ncu_traffic(w.name)
-    part_bytes = st["partial_rows"] * (128 * 4 + 4) * 2  # fp32 partial O + lse, written then read
-    slots = {"row8_kernel": st["unique_slots_row8"], "row_kernel": st["unique_slots_row32"]}
-    present = [st["num_items_row8"] > 0, st["num_items_rows"] > st["num_items_row8"],
-               st["num_items_tensor"] > 0, st["merge_rows"] > 0]
-    kernels = {}
-    for j, n in enumerate(names):
-        if not present[j]:
-            continue
-        if n == "tcgen05_kernel":
-            alg, unit, peak, pk, bound = st["flops_tensor"], "TFLOP/s", tflops_peak, tpeak_kind, "tensor"
-            scale = 1e12
-        else:
-            alg = (slots[n] * w.num_kv_heads * KV_BYTES_PER_SLOT_HEAD if n in slots
-                   else part_bytes // 2 + st["merge_rows"] * (128 * 2 + 4))
-            unit, peak, pk, bound, scale = "GB/s", hbm_peak, peak_kind, "hbm", 1e9
-        ach = alg / (avg[j] * 1e-3) / scale
-        kernels[n] = {"bound": bound, "achieved": ach, "peak": peak, "unit": unit,
-                      "frac": ach / peak, "ms": avg[j], "peak_kind": pk, "algorithmic": alg,
-                      "traffic": traffic.get(n)}
+
+def run_ours(args):
+    dist, rank, world, local = dist_setup(args.gpus)
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    K = args.steps
+    head = measure_config(args.config, args, dev, flush, dist, rank, world, K, keep=True)
+    w, run, st, unique_bytes = head["w"], head["run"], head["stats"], head["unique_bytes"]
+    stream = torch.cuda.current_stream(dev)
+    q, k, v = w.q, w.k_pages, w.v_pages
+    kernels = head["kernels"]
     dom = max(kernels, key=lambda n: kernels[n]["ms"])
     roof = dict(kernels[dom])
     roof["kernel"] = dom
@@ -397,6 +449,7 @@ def run_ours(args):
 
     cpu = None
     if not args.no_cpu_baseline and rank == 0 and world == 1:
+        import oracle
         hw = W.Workload(**{f: getattr(w, f) for f in ("name", "num_q_heads", "num_kv_heads", "page_ids", "segs",
                                                        "branch_seg_off", "branch_segs", "branch_q_off",
                                                        "vis_bits", "vis_word_off", "num_pages_pool")},
@@ -408,33 +461,55 @@ def run_ours(args):
                "kind": "oracle", "branch_queries_per_s": nq / secs,
                "sample": f"{nb} of {w.num_branches} branches (all heads), fp64 copied-context "
                          f"attention, {secs:.1f} s; GB/s prorated by the share of query tokens"}
+        # the tiny fork workload on one host core, whole (all 4 branches, all heads)
+        w1 = W.make(1)
+        t0 = time.perf_counter()
+        oracle.fork_attn(w1, threads=1)
+        s1 = time.perf_counter() - t0
+        u1 = oracle.unique_slots(w1)[0] * w1.num_kv_heads * KV_BYTES_PER_SLOT_HEAD
+        cpu["single_core"] = {"workload": w1.name, "seconds": s1, "cores": 1,
+                              "branch_queries_per_s": w1.total_q / s1,
+                              "value": u1 / s1 / 1e9, "unit": "GB/s"}
+
+    # the other workloads, each its own timed region with its own clock record
+    per_config = {}
+    if not args.no_per_config:
+        del q, k, v
+        for cfg in sorted(W.CONFIGS):
+            r = head if cfg == args.config else measure_config(cfg, args, dev, flush, dist, rank,
+                                                               world, K)
+            per_config[str(cfg)] = {
+                "workload": r["config"]["workload"], "value": r["value"], "unit": "GB/s",
+                "frac_of_hbm_peak": r["frac"], "branch_queries_per_s": r["bq_s"],
+                "ms_per_step": r["ms"], "step_ms_median": statistics.median(r["step_ms"]),
+                "kernel_ms": r["kernel_ms"], "unique_kv_bytes": r["unique_bytes"],
+                "tensor_ctas": r["stats"]["tensor_ctas"], "clocks": r["clocks"],
+                "steps": K}
 
     if rank == 0:
         line = {
-            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
-            "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
+            "metric": METRIC, "value": head["value"], "unit": "GB/s", "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": head["ms"], "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": w.name, "config_id": args.config, "Hq": w.num_q_heads,
-                       "Hkv": w.num_kv_heads, "branches": w.num_branches, "total_q": w.total_q,
-                       "unique_kv_bytes": unique_bytes, "l2": "flushed (256 MiB write) between steps",
-                       "plan_s": plan_s},
-            "branch_queries_per_s": bq_s,
-            "frac_of_hbm_peak": value / world / hbm_peak,
+            "config": head["config"],
+            "plan_s": head["plan_s"],
+            "branch_queries_per_s": head["bq_s"],
+            "frac_of_hbm_peak": head["frac"],
             "roofline": roof,
             "kernels": kernels,
-            "kernel_ms": {n: a for n, a, p in zip(names, avg, present) if p},
-            "per_kernel_timing": f"each kernel alone: CUDA events on the launching stream over {Kk} "
-                                 f"steps of the decode with its kernels one after another; in the "
-                                 f"timed region they overlap",
-            "step_ms_min": min(step_ms), "step_ms_median": statistics.median(step_ms),
-            "wall_s_timed_region": wall,
+            "kernel_ms": head["kernel_ms"],
+            "per_kernel_timing": f"each kernel alone: CUDA events on the launching stream over "
+                                 f"{head['Kk']} steps of the decode with its kernels one after "
+                                 f"another; in the timed region they overlap",
+            "step_ms_min": min(head["step_ms"]), "step_ms_median": statistics.median(head["step_ms"]),
+            "wall_s_timed_region": head["wall"],
             "tensor_ctas": st["tensor_ctas"],
-            "gpu_launches": K * (int(st["num_items_row8"] > 0) + int(st["num_items_rows"] > st["num_items_row8"])
-                                 + int(st["num_items_tensor"] > 0) + int(st["merge_rows"] > 0)),
+            "gpu_launches": K * head["launches_per_step"],
             "flops_per_step": st["flops_rows"] + st["flops_tensor"],
-            "clocks": clk.record(),
+            "clocks": head["clocks"],
             "e2e": e2e,
             "cpu_baseline": cpu,
+            "per_config": per_config,
             "gpu": torch.cuda.get_device_name(dev),
         }
         print(json.dumps(line), flush=True)
@@ -508,6 +583,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="time only --config (the line's per_config then stays empty)")
     ap.add_argument("--compact", action="store_true",
                     help="time the compaction op (8 branches of --config) instead of the decode")
     args = ap.parse_args()

@@ -141,8 +141,8 @@ typedef struct {
     int64_t total_q;
     int64_t unique_slots_rows;     /* distinct visible physical slots read by the row kernel */
     int64_t unique_slots_tensor;   /* distinct visible physical slots read by tcgen05 kernel */
-    int64_t flops_rows;            /* algorithmic flops of the row kernel: per visible slot  */
-    int64_t flops_tensor;          /* of a reader, 4 x 128 x (query rows) per KV head        */
+    int64_t flops_rows;            /* algorithmic flops of the row kernel: 4 x 128 per       */
+    int64_t flops_tensor;          /* (query row, KV head, visible slot causally before it)  */
     int64_t num_items_row8;        /* of num_items_rows: items with <= 8 rows (own kernel)   */
     int64_t unique_slots_row8;     /* visible slots of the chunks that kernel reads          */
     int64_t unique_slots_row32;    /* the same for the row kernel of up to 32 rows (a chunk  */
@@ -209,9 +209,15 @@ int fork_attn_decode_timed(const void *q, const void *k_pages, const void *v_pag
                            const fa_plan *plan, void *out, float *lse, void *stream,
                            void **events, int32_t n_events);
 
-/* Reads the plan's device error word on `stream` (synchronising it) into *device_error [host]
- * and clears it.  A non-zero word means a kernel gave up (an expired wait or a failed check)
- * and the outputs of that decode are not valid. */
+/* Reads the device error word of the plan's last decode on `stream` (synchronising it) into
+ * *device_error [host] and clears it.  A non-zero word means a kernel gave up (an expired wait
+ * or a failed check) and the outputs of that decode are not valid.  After
+ * fork_attn_plan_upload or fork_attn_decode(_timed) the word is the one in the plan buffer;
+ * after fork_attn_decode_static_scratch it is the one in the library's built-in device array
+ * on the device that call ran on (make that device current), which the next
+ * fork_attn_decode_static_scratch of any plan on that device overwrites.  Nothing is
+ * allocated.  Errors: FA_ERR_NULL, FA_ERR_NOT_UPLOADED (the plan was never uploaded nor run
+ * through fork_attn_decode_static_scratch), FA_ERR_CUDA, FA_ERR_DEVICE (the word was set). */
 int fork_attn_check(fa_plan *plan, int32_t *device_error, void *stream);
 
 /* Size of the device array used by fork_attn_decode_static_scratch: 32 MiB. */
@@ -236,8 +242,8 @@ int fork_attn_check(fa_plan *plan, int32_t *device_error, void *stream);
  * address with cudaGetSymbolAddress; make that first call before any stream capture.
  * Every call on a device shares the one array and leaves the last call's contents in it:
  * two calls whose work overlaps on the GPU (different streams, or different host threads)
- * race on it, so serialise them.  The device error word of these calls is not readable
- * through fork_attn_check.
+ * race on it, so serialise them.  fork_attn_check on the same plan reads and clears the
+ * device error word this call wrote (word 0 of the array), until another call overwrites it.
  *
  * Errors: FA_ERR_NULL, FA_ERR_ALIGN (as fork_attn_decode), FA_ERR_SCRATCH_LIMIT when
  * plan_bytes + scratch_bytes of fork_attn_plan_sizes exceed FA_STATIC_SCRATCH_BYTES (checked

@@ -214,6 +214,7 @@ extern "C" int fork_attn_plan_upload(fa_plan *plan, void *dev_plan_buf, size_t p
     plan->dev_plan = dev_plan_buf;
     plan->dev_scratch = dev_scratch_buf;
     plan->uploaded = true;
+    plan->err_word = static_cast<int32_t *>(dev_plan_buf);
     return FA_OK;
 }
 
@@ -246,20 +247,21 @@ extern "C" int fork_attn_decode(const void *q, const void *k_pages, const void *
     fa::DecodeParams p;
     rc = fill_params(plan, q, k_pages, v_pages, out, lse, plan->dev_scratch, p);
     if (rc != FA_OK) return rc;
+    plan->err_word = static_cast<int32_t *>(plan->dev_plan);
     return launch_all(p, plan, static_cast<cudaStream_t>(stream), nullptr, true);
 }
 
 extern "C" int fork_attn_check(fa_plan *plan, int32_t *device_error, void *stream) {
     if (!plan || !device_error) return FA_ERR_NULL;
-    if (!plan->uploaded) return FA_ERR_NOT_UPLOADED;
+    if (!plan->err_word) return FA_ERR_NOT_UPLOADED;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     int32_t word = 0;
-    if (cudaMemcpyAsync(&word, plan->dev_plan, sizeof word, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+    if (cudaMemcpyAsync(&word, plan->err_word, sizeof word, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
         cudaStreamSynchronize(st) != cudaSuccess)
         return FA_ERR_CUDA;
     *device_error = word;
     if (word != 0) {
-        if (cudaMemsetAsync(plan->dev_plan, 0, sizeof word, st) != cudaSuccess) return FA_ERR_CUDA;
+        if (cudaMemsetAsync(plan->err_word, 0, sizeof word, st) != cudaSuccess) return FA_ERR_CUDA;
         return FA_ERR_DEVICE;
     }
     return FA_OK;
@@ -329,5 +331,6 @@ extern "C" int fork_attn_decode_static_scratch(const void *q, const void *k_page
     p.merge_bases = reinterpret_cast<const int32_t *>(base + L.merge_bases);
     p.mask_words = reinterpret_cast<const uint32_t *>(base + L.mask_words);
     p.err = reinterpret_cast<int32_t *>(base);
+    plan->err_word = p.err;  // fork_attn_check reads this call's error word
     return launch_all(p, plan, st, nullptr, true);  // nothing is created here
 }

@@ -356,12 +356,19 @@ int build_plan(Input &in, const fa_plan_opts &opts, fa_plan *plan) {
                 st.touched_pages += 1;
                 for (int32_t t = 0; t < n_read; ++t) {
                     const Rec &rd = bd.recs[bd.by_page[bd.group_start[g] + t]];
-                    const int64_t seen = __builtin_popcount(rd.vis);
-                    st.listed_visible_slots += seen;
-                    // QK^T and P V: 2 x 128 multiply-adds per visible slot, query row and KV head
-                    const int64_t fl = seen * int64_t(in.q_off[rd.branch + 1] - in.q_off[rd.branch]) * G * Hkv * 4 *
-                                       fa::kHeadDim;
-                    (tc_run ? st.flops_tensor : st.flops_rows) += fl;
+                    st.listed_visible_slots += __builtin_popcount(rd.vis);
+                    // QK^T and P V: 2 x 128 multiply-adds per (query row, KV head, visible slot
+                    // at or before the query token's position); query tokens from the first
+                    // one whose position is past the page's last slot see all of its slots
+                    const int64_t nq = in.q_off[rd.branch + 1] - in.q_off[rd.branch];
+                    const int64_t qpos0 = in.n_b[rd.branch] - nq;
+                    const int64_t i_full = std::min<int64_t>(nq, std::max<int64_t>(0, int64_t(rd.lpos0) + kPageSize - 1 - qpos0));
+                    int64_t pairs = (nq - i_full) * __builtin_popcount(rd.vis);
+                    for (int64_t i = 0; i < i_full; ++i) {
+                        const int64_t cut = qpos0 + i - rd.lpos0;  // slots s <= cut are causally visible
+                        if (cut >= 0) pairs += __builtin_popcount(rd.vis & ((2u << cut) - 1u));
+                    }
+                    (tc_run ? st.flops_tensor : st.flops_rows) += pairs * G * Hkv * 4 * fa::kHeadDim;
                 }
             }
             for (int32_t t = 0; t < n_read; ++t) {
@@ -627,6 +634,7 @@ extern "C" int fork_attn_plan_create(const fa_dims *dims, const fa_desc *desc,
         p->dev_plan = nullptr;
         p->dev_scratch = nullptr;
         p->uploaded = false;
+        p->err_word = nullptr;
         rc = build_plan(in, o, p);
         if (rc != FA_OK) {
             delete p;

@@ -20,6 +20,10 @@ struct fa_plan {
     void *dev_plan;
     void *dev_scratch;
     bool uploaded;
+    // device error word of the plan's last decode: word 0 of dev_plan after an upload or a
+    // fork_attn_decode, word 0 of the built-in static array after a
+    // fork_attn_decode_static_scratch (read and cleared by fork_attn_check)
+    mutable int32_t *err_word;
 };
 
 namespace fa {

@@ -81,8 +81,8 @@ struct QMerge {
 
 // Byte offsets of the arrays inside the device plan buffer.  The first 256 bytes are a
 // header of int32 words, zero in the uploaded plan: [0] the device error word, [1] [2] the
-// work counter and exit count of the persistent tcgen05 kernel, [3] [4] those of the
-// persistent row kernel for <= 8 rows (each kernel's last CTA puts its pair back to zero).
+// work counter and exit count of the persistent tcgen05 kernel (its last CTA puts both back
+// to zero); the other words are unused and stay zero.
 struct Layout {
     int64_t chunk_pages, chunks, items_rows, items_tc, items_r8, rows, branches, q_merge, merge_bases,
         mask_words, total;
