@@ -107,7 +107,8 @@ typedef struct {
     const int64_t *vis_word_off;    /* j/32 for logical index j of branch b; 1 = visible.    */
                                     /* Both NULL = everything visible.                        */
     int64_t num_vis_words;          /* length of vis_bits (bounds vis_word_off[b] + n_b/32)  */
-    int64_t num_pages_pool;         /* physical page ids must lie in [0, num_pages_pool)     */
+    int64_t num_pages_pool;         /* physical page ids must lie in [0, num_pages_pool);    */
+                                    /* (num_pages_pool + 1) x num_kv_heads < 2^31             */
 } fa_desc;
 
 /* Planner knobs; pass NULL to fork_attn_plan_create for the defaults (all fields 0). */

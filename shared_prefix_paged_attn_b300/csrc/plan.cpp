@@ -68,6 +68,8 @@ int validate(Input &in) {
     if (s->num_branches < 1 || s->num_pages_pool < 1 || s->num_segs < 0 || s->num_page_ids < 0)
         return FA_ERR_INVALID;
     if (s->num_pages_pool > (int64_t(1) << 31) - 1) return FA_ERR_RANGE;
+    // the kernels address a page-head as page x Hkv + head in int32, one page past the pool too
+    if ((s->num_pages_pool + 1) * int64_t(d->num_kv_heads) > (int64_t(1) << 31) - 1) return FA_ERR_RANGE;
     if (!s->branch_seg_off || !s->branch_segs) return FA_ERR_NULL;
     if ((s->num_segs > 0 && !s->segs) || (s->num_page_ids > 0 && !s->page_ids)) return FA_ERR_NULL;
     if ((s->vis_bits == nullptr) != (s->vis_word_off == nullptr)) return FA_ERR_INVALID;

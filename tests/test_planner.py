@@ -83,6 +83,9 @@ def test_validation_errors():
         assert _plan_rc(variant(vis_bits=good.vis_bits[:1])) == -4
     for hq, hkv, rc in ((6, 4, -3), (64, 1, -3)):
         assert _plan_rc(variant(num_q_heads=hq, num_kv_heads=hkv)) == rc
+    # a page-head index (page x Hkv + head, one page past the pool too) must fit in int32
+    assert _plan_rc(variant(num_q_heads=1 << 16, num_kv_heads=1 << 16, num_pages_pool=(1 << 15) - 2)) == 0
+    assert _plan_rc(variant(num_q_heads=1 << 16, num_kv_heads=1 << 16, num_pages_pool=(1 << 15) - 1)) == -4
     for knob in ("chunk_pages", "num_sms", "tensor_ctas", "tensor_chunk_pages"):
         assert _plan_rc(good, **{knob: -1}) == -2
 
