@@ -32,21 +32,18 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// K pages [pool][Hkv][16][128] bf16 seen as a 5-D tensor (dims innermost first): 64 dims of a
-// half, 8 tokens of a group, 2 dim-halves, 2 token groups, and page x Hkv + head.  One box of
-// 64 x 8 x 2 x 2 lands a whole page-head (4 KiB) in shared memory as [group][half][8 tokens][64
-// dims], 128-byte swizzled: within a tile of pages placed 4 KiB apart, every 8-token group of
-// a dim-half then sits at a uniform 2 KiB stride, which is what a K-major MMA operand needs,
-// and a page costs one copy instead of two.  The page-head index must fit in int32 (checked).
-bool encode_pages_grouped(CUtensorMap *map, const void *pages, int64_t pool, int32_t hkv) {
+// Pages [pool][Hkv][16][128] bf16 seen as a 4-D tensor (dims innermost first), read in boxes
+// of 64 dims x 16 tokens of one head of one page, 128-byte swizzled in shared memory.
+bool encode_pages(CUtensorMap *map, const void *pages, int64_t pool, int32_t hkv) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
-    const cuuint64_t dims[5] = {64, 8, 2, 2, cuuint64_t(pool) * cuuint64_t(hkv)};
-    const cuuint64_t strides[4] = {cuuint64_t(fa::kHeadDim * 2), 128, 8 * cuuint64_t(fa::kHeadDim * 2),
-                                   cuuint64_t(fa::kPageSize * fa::kHeadDim * 2)};
-    const cuuint32_t box[5] = {64, 8, 2, 2, 1};
-    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(pages), dims, strides, box, estr,
+    const cuuint64_t dims[4] = {cuuint64_t(fa::kHeadDim), cuuint64_t(fa::kPageSize), cuuint64_t(hkv),
+                                cuuint64_t(pool)};
+    const cuuint64_t strides[3] = {cuuint64_t(fa::kHeadDim * 2), cuuint64_t(fa::kPageSize * fa::kHeadDim * 2),
+                                   cuuint64_t(hkv) * fa::kPageSize * fa::kHeadDim * 2};
+    const cuuint32_t box[4] = {64, cuuint32_t(fa::kPageSize), 1, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(pages), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -100,7 +97,8 @@ int set_smem_attr() {
 int fill_params(const fa_plan *plan, const void *q, const void *k_pages, const void *v_pages, void *out,
                 float *lse, void *scratch, fa::DecodeParams &p) {
     std::memset(&p, 0, sizeof p);
-    if (!encode_pages_grouped(&p.kmap_grp, k_pages, plan->num_pages_pool, plan->dims.num_kv_heads) ||
+    if (!encode_pages(&p.kmap, k_pages, plan->num_pages_pool, plan->dims.num_kv_heads) ||
+        !encode_pages(&p.vmap, v_pages, plan->num_pages_pool, plan->dims.num_kv_heads) ||
         !encode_pages_whole(&p.kmap_page, k_pages, plan->num_pages_pool, plan->dims.num_kv_heads) ||
         !encode_pages_whole(&p.vmap_page, v_pages, plan->num_pages_pool, plan->dims.num_kv_heads))
         return FA_ERR_CUDA;

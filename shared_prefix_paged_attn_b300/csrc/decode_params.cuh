@@ -9,8 +9,8 @@
 namespace fa {
 
 struct DecodeParams {
-    CUtensorMap kmap_grp;   // K as [page x Hkv + head][2 groups of 8 tokens][2 halves][8][64]:
-                            // one box = a whole page-head (the tcgen05 kernel's K)
+    CUtensorMap kmap;  // K pages viewed as [pages][Hkv][16][128] bf16, box 64 x 16, 128B swizzle
+    CUtensorMap vmap;  // same for V
     CUtensorMap kmap_page;  // K as [pages][Hkv][2 halves][16][64]: one box = a whole page-head
     CUtensorMap vmap_page;  // V the same way
     const __nv_bfloat16 *q;

@@ -37,6 +37,9 @@ namespace {
 
 using fa::kPageSize;
 
+// Time of one 128-token tile of a tcgen05 work item on B300 (microseconds), for the CTA split.
+constexpr double kTcTileUs = 2.2;
+
 struct Rec {
     int32_t page;
     int32_t branch;
@@ -505,9 +508,8 @@ int build_plan(Input &in, const fa_plan_opts &opts, fa_plan *plan) {
     // counter runs dry).  For every candidate count n the planner replays the device's work
     // counter -- items in queue order, each to the CTA that frees first -- and lets the row
     // work stream on the SMs left and freed, then keeps the n whose last kernel ends first.
-    // Rates measured on B300: a tcgen05 item costs about 2.2 us per 128-token tile (one M
-    // tile or two: the per-tile chain is the softmax's) plus 2 us; row work streams about
-    // 85 GB/s per SM beside it and at most 6.2 TB/s in all.  fa_plan_opts.tensor_ctas > 0
+    // Rates measured on B300: a tcgen05 item costs about kTcTileUs per 128-token tile plus
+    // 2 us; row work streams about 85 GB/s per SM beside it and at most 6.2 TB/s in all.  fa_plan_opts.tensor_ctas > 0
     // overrides the choice.
     {
         const int sms = opts.num_sms > 0 ? opts.num_sms : 148;
@@ -515,7 +517,7 @@ int build_plan(Input &in, const fa_plan_opts &opts, fa_plan *plan) {
         if (!em.items_tc.empty() && st.kv_bytes_rows > 0) {
             std::vector<double> cost(em.items_tc.size());
             for (size_t i = 0; i < em.items_tc.size(); ++i)
-                cost[i] = 2.2e-6 * double((em.chunks[em.items_tc[i].chunk].n_pages + 7) / 8) + 2e-6;
+                cost[i] = kTcTileUs * 1e-6 * double((em.chunks[em.items_tc[i].chunk].n_pages + 7) / 8) + 2e-6;
             const double row_bytes = double(st.kv_bytes_rows), rate_sm = 85e9, rate_all = 6.2e12;
             double t_best = 1e30;
             std::vector<double> fin;

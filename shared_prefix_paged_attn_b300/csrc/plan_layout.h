@@ -90,10 +90,13 @@ struct Layout {
         n_merge_bases, n_mask_words;
 };
 
-// Device error word bits.
+// Device error word bits (header word 0), and which kernel set them.
 enum : int32_t {
     kErrTimeout = 1,   // a bounded wait expired
     kErrBounds = 2,    // a checked index was out of range
+    kErrTc = 4,        // ... in the tcgen05 kernel
+    kErrRow8 = 8,      // ... in the row kernel for <= 8 rows
+    kErrRow = 16,      // ... in the row kernel for <= 32 rows
 };
 
 }  // namespace fa

@@ -247,7 +247,7 @@ __global__ void __launch_bounds__(kThreads, 3) row8_kernel(const __grid_constant
         // give the copies still in flight a bounded chance to land before the smem is reused
         for (int jj = j + 1; jj < issued; ++jj)
             ptx::mbar_wait(ptx::smem_u32(&sm.bars[warp][jj % kStages]), (jj / kStages) & 1);
-        if (lane == 0) atomicOr(p.err, kErrTimeout);
+        if (lane == 0) atomicOr(p.err, kErrTimeout | kErrRow8);
     }
 
     // ---- combine the four warps ----

@@ -252,7 +252,7 @@ __device__ __forceinline__ void run_pages(const DecodeParams &p, Smem &sm, const
         // give the copies still in flight a bounded chance to land before the smem is reused
         for (int jj = j + 1; jj < issued; ++jj)
             ptx::mbar_wait(ptx::smem_u32(&sm.bars[warp][jj % kStages]), (jj / kStages) & 1);
-        if (lane == 0) atomicOr(p.err, kErrTimeout);
+        if (lane == 0) atomicOr(p.err, kErrTimeout | kErrRow);
     }
 }
 
