@@ -205,16 +205,32 @@ def dist_setup(n_gpus):
     return None, 0, 1, 0
 
 
-def rank_workload(config, rank, device, values=True):
-    """Rank r's problem: the workload's structure with values drawn from seed + 1000 r (the
-    decode shards into independent problems, one per GPU: weak scaling, no collective on the
-    data path)."""
+def rank_workload(config, rank, device, values=True, split="none", world=1):
+    """Rank r's problem.  split "none": the workload's structure with values drawn from
+    seed + 1000 r (independent problems, one per GPU: weak scaling).  split "head" or
+    "request": rank r's share of the one workload, by KV head or by request (strong
+    scaling).  Neither has a collective on the data path."""
+    if split != "none" and world > 1:
+        from shared_prefix_paged_attn_b300 import shard
+        w = W.make(config, device=device, values=values)
+        cid = config
+        w = shard.split_by_kv_head(w, rank, world) if split == "head" else shard.split_by_request(w, rank, world)[0]
+        w.meta["config_id"] = cid
+        return w
     w = W.make(config, device=device, values=values and rank == 0)
     if rank:
         w.meta["seed"] += 1000 * rank
         if values:
             W.fill_values(w, device=device)
     return w
+
+
+def sum_over_ranks(dist, x, device):
+    if dist is None:
+        return x
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
 
 
 def max_over_ranks(dist, ms, device):
@@ -333,7 +349,8 @@ def measure_config(cfg, args, dev, flush, dist, rank, world, steps, keep=False):
     the launching stream, clocks sampled) and then the same number of one-by-one decodes for
     the per-kernel times.  Returns a dict; with keep=True it also holds the workload and the
     ForkAttention object (for the end-to-end and CPU legs)."""
-    w = rank_workload(cfg, rank, str(dev))
+    split = getattr(args, "split", "none")
+    w = rank_workload(cfg, rank, str(dev), split=split, world=world)
     w.meta["config_id"] = cfg
     t0 = time.perf_counter()
     run = fa.ForkAttention(w, out_dtype=fa.FA_BF16, device=dev)
@@ -393,10 +410,14 @@ def measure_config(cfg, args, dev, flush, dist, rank, world, steps, keep=False):
            for j in range(len(KERNEL_NAMES))]
     kernels = kernel_rooflines(st, w, avg, ncu_traffic(w.name))
     hbm_peak, _ = peaks()
-    value = unique_bytes * world / (ms_max * 1e-3) / 1e9
+    # whole-job unique KV bytes: every rank's own problem (weak), or the shares of one
+    # problem, which add up to it (strong)
+    job_bytes = unique_bytes * world if split == "none" else sum_over_ranks(dist, unique_bytes, dev)
+    job_q = w.total_q * world if split == "none" else sum_over_ranks(dist, w.total_q, dev)
+    value = job_bytes / (ms_max * 1e-3) / 1e9
     res = {"cfg": cfg, "w": w if keep else None, "run": run if keep else None, "stats": st,
            "unique_bytes": unique_bytes, "plan_s": plan_s, "ms": ms_max, "step_ms": step_ms,
-           "wall": wall, "value": value, "bq_s": w.total_q * world / (ms_max * 1e-3),
+           "wall": wall, "value": value, "bq_s": job_q / (ms_max * 1e-3),
            "frac": value / world / hbm_peak, "kernels": kernels,
            "kernel_ms": {n: a for n, a, p in zip(KERNEL_NAMES, avg, kernels_present(st)) if p},
            "clocks": clk.record(), "config": workload_config(w, unique_bytes), "Kk": Kk,
@@ -476,8 +497,12 @@ def run_ours(args):
     if not args.no_per_config:
         del q, k, v
         for cfg in sorted(W.CONFIGS):
-            r = head if cfg == args.config else measure_config(cfg, args, dev, flush, dist, rank,
-                                                               world, K)
+            try:
+                r = head if cfg == args.config else measure_config(cfg, args, dev, flush, dist, rank,
+                                                                   world, K)
+            except ValueError as e:  # a split this workload does not have (one request)
+                per_config[str(cfg)] = {"skipped": str(e)}
+                continue
             per_config[str(cfg)] = {
                 "workload": r["config"]["workload"], "value": r["value"], "unit": "GB/s",
                 "frac_of_hbm_peak": r["frac"], "branch_queries_per_s": r["bq_s"],
@@ -486,11 +511,38 @@ def run_ours(args):
                 "tensor_ctas": r["stats"]["tensor_ctas"], "clocks": r["clocks"],
                 "steps": K}
 
+    # the packed DAG prefill (every token a query): tensor-bound, so its figure is the
+    # causally visible flops per second against the dense bf16 peak
+    prefill = None
+    r = None
+    if not args.no_prefill:
+        try:
+            r = measure_config(W.PREFILL, args, dev, flush, dist, rank, world, max(3, min(K, 20)))
+        except ValueError as e:  # a split this workload does not have (one request)
+            prefill = {"skipped": str(e)}
+    if r is not None:
+        rs = r["stats"]
+        flops = rs["flops_rows"] + rs["flops_tensor"]
+        tpk, tpk_kind = tensor_peak()
+        job_flops = flops * world if args.split == "none" else sum_over_ranks(dist, flops, dev)
+        tfl = job_flops / (r["ms"] * 1e-3) / 1e12
+        prefill = {"workload": r["config"]["workload"], "metric": "causal attention TFLOP/s",
+                   "value": tfl, "unit": "TFLOP/s", "frac_of_bf16_peak": tfl / world / tpk,
+                   "peak": tpk, "peak_kind": tpk_kind, "flops_per_step": flops,
+                   "flops_counted": "4 x 128 per (query row, KV head, visible key at or before "
+                                    "the query's position): causal pairs only",
+                   "ms_per_step": r["ms"], "step_ms_median": statistics.median(r["step_ms"]),
+                   "total_q": r["config"]["total_q"], "kernel_ms": r["kernel_ms"],
+                   "kernels": r["kernels"], "items_skipped": rs["items_skipped"],
+                   "tensor_ctas": rs["tensor_ctas"], "clocks": r["clocks"],
+                   "steps": max(3, min(K, 20)), "gpu_launches": max(3, min(K, 20)) * r["launches_per_step"]}
+
     if rank == 0:
         line = {
             "metric": METRIC, "value": head["value"], "unit": "GB/s", "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": head["ms"], "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "scaling": "weak" if args.split == "none" else "strong", "split": args.split,
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": head["config"],
             "plan_s": head["plan_s"],
             "branch_queries_per_s": head["bq_s"],
@@ -510,6 +562,7 @@ def run_ours(args):
             "e2e": e2e,
             "cpu_baseline": cpu,
             "per_config": per_config,
+            "packed_dag_prefill": prefill,
             "gpu": torch.cuda.get_device_name(dev),
         }
         print(json.dumps(line), flush=True)
@@ -518,9 +571,10 @@ def run_ours(args):
 
 
 def run_compact(args):
-    """Physical compaction (with and without repositioning) of the first 8 branches of the
-    workload into fresh pages of a grown pool; one JSON line per mode.  Bytes per launch: the
-    kept entries' K and V read and written (kept x Hkv x 512 B x 2)."""
+    """Physical compaction (with and without repositioning, each branch on its own or the
+    common prefix once) of the first 8 branches of the workload into fresh pages of a grown
+    pool; one JSON line per mode.  Bytes per launch: the moved entries' K and V read and
+    written (moved x Hkv x 512 B x 2)."""
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     w = W.make(args.config, device=str(dev))
@@ -539,12 +593,14 @@ def run_compact(args):
     fresh = np.arange(pool, pool + need, dtype=np.int32)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     hbm_peak, peak_kind = peaks()
-    for rep in (False, True):
+    for rep, share in ((False, False), (True, False), (False, True), (True, True)):
         t0 = time.perf_counter()
-        plan = fa.fork_attn_compact_create(w, branches, fresh, reposition=rep)
+        plan = fa.fork_attn_compact_create(w, branches, fresh, reposition=rep, share_prefix=share)
         plan_s = time.perf_counter() - t0
         kept, wb = plan.sizes()
-        moved = int(kept.sum()) * w.num_kv_heads * KV_BYTES_PER_SLOT_HEAD * 2
+        rs, _ = plan.shared()
+        entries = rs + int((kept - rs).sum())  # entries moved: the shared run once
+        moved = entries * w.num_kv_heads * KV_BYTES_PER_SLOT_HEAD * 2
         work = torch.empty(wb // 4 + 64, dtype=torch.int32, device=dev)
         fa.fork_attn_compact_upload(plan, work)
         for _ in range(args.warmup):
@@ -562,10 +618,12 @@ def run_compact(args):
         med = ms[len(ms) // 2]
         gbs = moved / (med * 1e-3) / 1e9
         print(json.dumps({"metric": "compaction: kept K/V bytes read + written per second", "op": "compact",
-                          "reposition": rep, "value": gbs, "unit": "GB/s", "ms_per_launch": med,
+                          "reposition": rep, "share_prefix": share, "value": gbs, "unit": "GB/s",
+                          "ms_per_launch": med,
                           "ms_min": ms[0], "steps": args.steps, "warmup": args.warmup,
                           "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
                           "config": {"workload": w.name, "branches": len(branches), "kept_tokens": int(kept.sum()),
+                                     "moved_entries": entries, "shared_kept": rs,
                                      "Hkv": w.num_kv_heads, "bytes_per_launch": moved,
                                      "l2": "flushed (256 MiB write) between launches", "plan_s": plan_s},
                           "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
@@ -585,6 +643,11 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-per-config", action="store_true",
                     help="time only --config (the line's per_config then stays empty)")
+    ap.add_argument("--split", choices=["none", "head", "request"], default="none",
+                    help="with N > 1: every rank its own problem (none, weak scaling) or a share "
+                         "of one problem by KV head or by request (strong scaling)")
+    ap.add_argument("--no-prefill", action="store_true",
+                    help="leave out the packed DAG prefill entry of the line")
     ap.add_argument("--compact", action="store_true",
                     help="time the compaction op (8 branches of --config) instead of the decode")
     args = ap.parse_args()

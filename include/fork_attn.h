@@ -149,6 +149,10 @@ typedef struct {
     int64_t unique_slots_row32;    /* the same for the row kernel of up to 32 rows (a chunk  */
                                    /* whose row groups go to both counts in both)            */
     int64_t tensor_ctas;           /* persistent CTAs the tcgen05 kernel is launched with    */
+    int64_t items_skipped;         /* (row group, chunk) pairs left out (any KV head): every */
+                                   /* row's query token lies before the chunk's first slot   */
+                                   /* (prefill-shaped plans); items read only up to the last */
+                                   /* page some row of the group can see                     */
 } fa_plan_stats;
 
 typedef struct fa_plan fa_plan; /* opaque; owned by the library */
@@ -265,26 +269,38 @@ int fork_attn_decode_static_scratch(const void *q, const void *k_pages, const vo
  * by the position change d = n - j: for i < head_dim / 2 with theta_i =
  * rope_base^(-2 i / head_dim), the pair (x_i, x_{i + head_dim/2}) becomes
  * (x_i cos(d theta_i) - x_{i+h} sin(d theta_i), x_{i+h} cos(d theta_i) + x_i sin(d theta_i))
- * (rotate-half pairing), computed in fp32 and rounded to bf16 (nearest even). */
+ * (rotate-half pairing), computed in fp32 and rounded to bf16 (nearest even).
+ *
+ * share_prefix != 0 keeps a fork's sharing: the listed branches' common prefix -- the first
+ * P logical entries, where every listed branch has the same physical slot and the same
+ * visibility bit at each of them -- is packed once, and each branch's entries after it go
+ * to pages of the branch's own.  Entry n of every branch is still the n-th kept one, with the
+ * same position change, so each branch reads [the shared run's r_s entries] then [its own
+ * r - r_s entries], two segments that both start at slot 0 of a page. */
 typedef struct {
     int32_t num_kv_heads;
     int32_t head_dim;     /* 128 */
     int32_t page_size;    /* 16 */
     int32_t reposition;   /* 0: keys copied; 1: keys rotated from position j to n (Repos) */
     double rope_base;     /* > 1; used when reposition != 0 */
+    int32_t share_prefix; /* 0: every branch packed on its own; 1: common prefix packed once */
+    int32_t reserved;     /* must be 0 */
 } fa_compact_dims;
 
 typedef struct fa_compact fa_compact; /* opaque; owned by the library */
 
 /* Plans the compaction of branches[0 .. num_branches) of `desc` (host arrays, read here
  * only).  Destination pages are dst_page_ids [host], consumed branch after branch, each branch
- * from a fresh page (ceil(r / page_size) pages for r kept entries).  They must not be pages of
+ * from a fresh page (ceil(r / page_size) pages for r kept entries); with share_prefix the
+ * shared run's ceil(r_s / page_size) pages come first, then each branch's ceil((r - r_s) /
+ * page_size).  They must not be pages of
  * any listed branch (the gather runs in place in the same pool) and must not hold anything
  * another reader still needs.  Errors: FA_ERR_NULL, FA_ERR_INVALID (branch index, bad CSR or
  * segment, too few destination pages, a destination page listed twice or read by a listed
- * branch, rope_base <= 1 with reposition), FA_ERR_RANGE (page id, segment id or bit word out
- * of range; a pool of more than 2^27 pages), FA_ERR_UNSUPPORTED (head_dim != 128, page_size
- * != 16), FA_ERR_NOMEM.  *out is set only on FA_OK. */
+ * branch, rope_base <= 1 with reposition, share_prefix not 0 or 1, reserved != 0),
+ * FA_ERR_RANGE (page id, segment id or bit word out of range; a pool of more than 2^27
+ * pages), FA_ERR_UNSUPPORTED (head_dim != 128, page_size != 16), FA_ERR_NOMEM.  *out is set
+ * only on FA_OK. */
 int fork_attn_compact_create(const fa_compact_dims *dims, const fa_desc *desc,
                              const int32_t *branches, int32_t num_branches,
                              const int32_t *dst_page_ids, int64_t num_dst_pages,
@@ -293,6 +309,11 @@ int fork_attn_compact_create(const fa_compact_dims *dims, const fa_desc *desc,
 /* kept_tokens [host, num_branches] (may be NULL): r per listed branch.  work_bytes (may be
  * NULL): the size of the device work buffer of fork_attn_compact_upload. */
 int fork_attn_compact_sizes(const fa_compact *c, int64_t *kept_tokens, size_t *work_bytes);
+
+/* shared_kept (may be NULL): r_s, the kept entries of the shared run (0 without
+ * share_prefix).  prefix_len (may be NULL): P, the common prefix's length in logical entries
+ * (0 without share_prefix). */
+int fork_attn_compact_shared(const fa_compact *c, int64_t *shared_kept, int64_t *prefix_len);
 
 /* Copies the plan's slot lists into dev_work [device, 256-byte aligned, >= work_bytes] on
  * `stream` (from the plan's host memory: keep the plan until the stream has passed the copy).

@@ -74,3 +74,22 @@ def compact(w, b, reposition=False, base=10000.0):
         delta = np.arange(len(kept), dtype=np.int64) - kept
         K = rope_rotate(K, delta[:, None], base)
     return K, V, kept
+
+
+def common_prefix(w, branches):
+    """(P, r_s): the listed branches' common prefix -- the first P logical indices at which
+    all of them have the same physical slot and the same visibility bit -- and the number of
+    kept entries in it.  A plain walk, one index at a time."""
+    if len(branches) == 0:
+        return 0, 0
+    slots = [branch_slots(w, b) for b in branches]
+    vis = []
+    for b, s in zip(branches, slots):
+        v = np.zeros(len(s), dtype=bool)
+        v[kept_indices(w, b)] = True
+        vis.append(v)
+    P = 0
+    while all(P < len(s) for s in slots) and \
+            all(slots[k][P] == slots[0][P] and vis[k][P] == vis[0][P] for k in range(len(slots))):
+        P += 1
+    return P, int(vis[0][:P].sum())

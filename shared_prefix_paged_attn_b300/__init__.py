@@ -213,6 +213,14 @@ class CompactPlan:
                "fork_attn_compact_sizes")
         return kept, wb.value
 
+    def shared(self):
+        """(r_s, P): kept entries of the shared run and the common prefix's length (0, 0
+        without share_prefix)."""
+        rs, pl = ctypes.c_int64(), ctypes.c_int64()
+        _check(_lib.load().fork_attn_compact_shared(self.handle, ctypes.byref(rs), ctypes.byref(pl)),
+               "fork_attn_compact_shared")
+        return rs.value, pl.value
+
     def destroy(self):
         if self.handle:
             _lib.load().fork_attn_compact_destroy(self.handle)
@@ -226,7 +234,7 @@ class CompactPlan:
 
 
 def fork_attn_compact_create(w, branches, dst_page_ids, reposition=False, rope_base=10000.0,
-                             head_dim=128, page_size=16) -> CompactPlan:
+                             head_dim=128, page_size=16, share_prefix=False) -> CompactPlan:
     """fork_attn_compact_create for a ``workloads.Workload``-like descriptor (host arrays)."""
     keep = []
 
@@ -240,7 +248,7 @@ def fork_attn_compact_create(w, branches, dst_page_ids, reposition=False, rope_b
     desc = _desc(arr, w.page_ids, w.segs, w.branch_seg_off, w.branch_segs, w.num_pages_pool,
                  w.branch_q_off, w.vis_bits, w.vis_word_off)
     dims = FaCompactDims(int(w.num_kv_heads), int(head_dim), int(page_size), int(bool(reposition)),
-                         float(rope_base))
+                         float(rope_base), int(bool(share_prefix)), 0)
     br = np.ascontiguousarray(branches, dtype=np.int32)
     dst = np.ascontiguousarray(dst_page_ids, dtype=np.int32)
     keep += [br, dst, desc, dims]

@@ -46,12 +46,14 @@ class FaPlanStats(ctypes.Structure):
                 ("unique_slots_rows", c_int64), ("unique_slots_tensor", c_int64),
                 ("flops_rows", c_int64), ("flops_tensor", c_int64),
                 ("num_items_row8", c_int64), ("unique_slots_row8", c_int64),
-                ("unique_slots_row32", c_int64), ("tensor_ctas", c_int64)]
+                ("unique_slots_row32", c_int64), ("tensor_ctas", c_int64),
+                ("items_skipped", c_int64)]
 
 
 class FaCompactDims(ctypes.Structure):
     _fields_ = [("num_kv_heads", c_int32), ("head_dim", c_int32), ("page_size", c_int32),
-                ("reposition", c_int32), ("rope_base", ctypes.c_double)]
+                ("reposition", c_int32), ("rope_base", ctypes.c_double),
+                ("share_prefix", c_int32), ("reserved", c_int32)]
 
 
 # name -> (restype, argtypes); every symbol declared in include/fork_attn.h
@@ -75,6 +77,7 @@ SIGNATURES = {
                                            c_void_p, c_int32, c_void_p, ctypes.c_int64,
                                            ctypes.POINTER(c_void_p)]),
     "fork_attn_compact_sizes": (c_int32, [c_void_p, c_void_p, ctypes.POINTER(ctypes.c_size_t)]),
+    "fork_attn_compact_shared": (c_int32, [c_void_p, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int64)]),
     "fork_attn_compact_upload": (c_int32, [c_void_p, c_void_p, ctypes.c_size_t, c_void_p]),
     "fork_attn_compact_run": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p]),
     "fork_attn_compact_destroy": (c_int32, [c_void_p]),

@@ -120,6 +120,7 @@ int fill_params(const fa_plan *plan, const void *q, const void *k_pages, const v
     p.branches = reinterpret_cast<const fa::Branch *>(base + L.branches);
     p.q_merge = reinterpret_cast<const fa::QMerge *>(base + L.q_merge);
     p.merge_bases = reinterpret_cast<const int32_t *>(base + L.merge_bases);
+    p.merge_lpos = reinterpret_cast<const int32_t *>(base + L.merge_lpos);
     p.mask_words = reinterpret_cast<const uint32_t *>(base + L.mask_words);
     p.err = reinterpret_cast<int32_t *>(base);
     p.Hq = plan->dims.num_q_heads;
@@ -329,6 +330,7 @@ extern "C" int fork_attn_decode_static_scratch(const void *q, const void *k_page
     p.branches = reinterpret_cast<const fa::Branch *>(base + L.branches);
     p.q_merge = reinterpret_cast<const fa::QMerge *>(base + L.q_merge);
     p.merge_bases = reinterpret_cast<const int32_t *>(base + L.merge_bases);
+    p.merge_lpos = reinterpret_cast<const int32_t *>(base + L.merge_lpos);
     p.mask_words = reinterpret_cast<const uint32_t *>(base + L.mask_words);
     p.err = reinterpret_cast<int32_t *>(base);
     plan->err_word = p.err;  // fork_attn_check reads this call's error word

@@ -27,6 +27,7 @@ struct DecodeParams {
     const Branch *branches;
     const QMerge *q_merge;
     const int32_t *merge_bases;
+    const int32_t *merge_lpos;  // first logical position of each partial's chunk
     const uint32_t *mask_words;
     int32_t *err;
     int32_t Hq, Hkv, G, out_dtype;

@@ -273,6 +273,7 @@ struct Emit {
     std::vector<fa::Branch> branches;
     std::vector<fa::QMerge> q_merge;
     std::vector<int32_t> merge_bases;
+    std::vector<int32_t> merge_lpos;  // first logical position of each partial's chunk
     std::vector<uint32_t> mask_words;
 };
 
@@ -369,7 +370,7 @@ int build_plan(Input &in, const fa_plan_opts &opts, fa_plan *plan) {
                     const int64_t qpos0 = in.n_b[rd.branch] - nq;
                     const int64_t i_full = std::min<int64_t>(nq, std::max<int64_t>(0, int64_t(rd.lpos0) + kPageSize - 1 - qpos0));
                     int64_t pairs = (nq - i_full) * __builtin_popcount(rd.vis);
-                    for (int64_t i = 0; i < i_full; ++i) {
+                    for (int64_t i = std::max<int64_t>(0, int64_t(rd.lpos0) - qpos0); i < i_full; ++i) {
                         const int64_t cut = qpos0 + i - rd.lpos0;  // slots s <= cut are causally visible
                         if (cut >= 0) pairs += __builtin_popcount(rd.vis & ((2u << cut) - 1u));
                     }
@@ -407,7 +408,7 @@ int build_plan(Input &in, const fa_plan_opts &opts, fa_plan *plan) {
 
     // partial rows: a branch read by a single occurrence writes `out` directly
     em.branches.resize(B);
-    std::vector<std::vector<int32_t>> per_branch(B);
+    std::vector<std::vector<int32_t>> per_branch(B), per_branch_lpos(B);
     int64_t prow = 0;
     for (size_t o = 0; o < em.occs.size(); ++o) {
         const int32_t b = em.occs[o].branch;
@@ -416,6 +417,7 @@ int build_plan(Input &in, const fa_plan_opts &opts, fa_plan *plan) {
         } else {
             em.occs[o].prow_base = int32_t(prow);
             per_branch[b].push_back(int32_t(prow));
+            per_branch_lpos[b].push_back(em.occs[o].lpos0);
             prow += int64_t(in.q_off[b + 1] - in.q_off[b]) * G * Hkv;
             if (prow > (int64_t(1) << 31) - 1) return FA_ERR_UNSUPPORTED;
         }
@@ -430,7 +432,21 @@ int build_plan(Input &in, const fa_plan_opts &opts, fa_plan *plan) {
         br.n_merge = int32_t(per_branch[b].size());
         br.direct = occ_count[b] == 1;
         em.merge_bases.insert(em.merge_bases.end(), per_branch[b].begin(), per_branch[b].end());
-        for (int32_t i = 0; i < br.n_q; ++i) em.q_merge.push_back(fa::QMerge{br.merge_off, br.n_merge, br.direct, i});
+        em.merge_lpos.insert(em.merge_lpos.end(), per_branch_lpos[b].begin(), per_branch_lpos[b].end());
+        for (int32_t i = 0; i < br.n_q; ++i) {
+            fa::QMerge qm;
+            std::memset(&qm, 0, sizeof qm);
+            qm.merge_off = br.merge_off;
+            qm.n_merge = br.n_merge;
+            qm.direct = br.direct;
+            qm.i = i;
+            qm.pos = br.qpos0 + i;
+            for (int32_t k = 0; k < std::min(br.n_merge, fa::kMergeInline); ++k) {
+                qm.base[k] = per_branch[b][k];
+                qm.lpos[k] = per_branch_lpos[b][k];
+            }
+            em.q_merge.push_back(qm);
+        }
         if (occ_count[b] != 1) st.merge_rows += int64_t(br.n_q) * in.d->num_q_heads;
     }
 
@@ -473,15 +489,29 @@ int build_plan(Input &in, const fa_plan_opts &opts, fa_plan *plan) {
             if (r8) st.unique_slots_row8 += chunk_slots[c];
             if (r32) st.unique_slots_row32 += chunk_slots[c];
         }
+        // pages each row group can see: up to its largest causal limit (a group whose rows all
+        // lie before the chunk sees nothing of it and gets no item at all)
+        std::vector<int32_t> group_pages(groups.size());
+        for (size_t gi = 0; gi < groups.size(); ++gi) {
+            int32_t lim = -1;
+            for (int32_t r = groups[gi].first; r < groups[gi].first + groups[gi].second; ++r)
+                lim = std::max(lim, em.rows[r].climit);
+            group_pages[gi] = lim < 0 ? 0 : int32_t(std::min<int64_t>(ch.n_pages, int64_t(lim) / kPageSize + 1));
+        }
         for (int32_t h = 0; h < Hkv; ++h) {
             for (size_t gi = 0; gi < groups.size(); ++gi) {
+                if (group_pages[gi] == 0) {
+                    if (h == 0) st.items_skipped += 1;
+                    continue;
+                }
                 fa::Item it;
                 std::memset(&it, 0, sizeof it);
                 it.chunk = int32_t(c);
                 it.head = h;
                 it.row_off = groups[gi].first;
                 it.n_rows = groups[gi].second;
-                const int64_t kv = int64_t(ch.n_pages) * kPageSize * fa::kHeadDim * 2 * 2;
+                it.n_pages = group_pages[gi];
+                const int64_t kv = int64_t(it.n_pages) * kPageSize * fa::kHeadDim * 2 * 2;
                 if (tc) {
                     em.items_tc.push_back(it);
                     st.kv_bytes_tensor += kv;
@@ -494,10 +524,10 @@ int build_plan(Input &in, const fa_plan_opts &opts, fa_plan *plan) {
         if (em.rows.size() > size_t(INT32_MAX)) return FA_ERR_UNSUPPORTED;
     }
 
-    // longest chunks first (stable, so a chunk's row groups and heads stay adjacent and share
+    // longest items first (stable, so a chunk's row groups and heads stay adjacent and share
     // its pages in L2): the last wave of CTAs is made of short items
     auto by_len = [&](const fa::Item &a, const fa::Item &b) {
-        return em.chunks[a.chunk].n_pages > em.chunks[b.chunk].n_pages;
+        return a.n_pages > b.n_pages;
     };
     std::stable_sort(em.items_tc.begin(), em.items_tc.end(), by_len);
     std::stable_sort(em.items_rows.begin(), em.items_rows.end(), by_len);
@@ -517,7 +547,7 @@ int build_plan(Input &in, const fa_plan_opts &opts, fa_plan *plan) {
         if (!em.items_tc.empty() && st.kv_bytes_rows > 0) {
             std::vector<double> cost(em.items_tc.size());
             for (size_t i = 0; i < em.items_tc.size(); ++i)
-                cost[i] = kTcTileUs * 1e-6 * double((em.chunks[em.items_tc[i].chunk].n_pages + 7) / 8) + 2e-6;
+                cost[i] = kTcTileUs * 1e-6 * double((em.items_tc[i].n_pages + 7) / 8) + 2e-6;
             const double row_bytes = double(st.kv_bytes_rows), rate_sm = 85e9, rate_all = 6.2e12;
             double t_best = 1e30;
             std::vector<double> fin;
@@ -588,6 +618,7 @@ int build_plan(Input &in, const fa_plan_opts &opts, fa_plan *plan) {
     L.branches = place(int64_t(em.branches.size()) * sizeof(fa::Branch));
     L.q_merge = place(int64_t(em.q_merge.size()) * sizeof(fa::QMerge));
     L.merge_bases = place(int64_t(em.merge_bases.size()) * 4);
+    L.merge_lpos = place(int64_t(em.merge_lpos.size()) * 4);
     L.mask_words = place(int64_t(em.mask_words.size()) * 4);
     L.total = off;
     L.n_chunk_pages = int32_t(em.chunk_pages.size());
@@ -611,6 +642,7 @@ int build_plan(Input &in, const fa_plan_opts &opts, fa_plan *plan) {
     put(L.branches, em.branches.data(), em.branches.size() * sizeof(fa::Branch));
     put(L.q_merge, em.q_merge.data(), em.q_merge.size() * sizeof(fa::QMerge));
     put(L.merge_bases, em.merge_bases.data(), em.merge_bases.size() * 4);
+    put(L.merge_lpos, em.merge_lpos.data(), em.merge_lpos.size() * 4);
     put(L.mask_words, em.mask_words.data(), em.mask_words.size() * 4);
     plan->partial_rows = prow;
     return FA_OK;

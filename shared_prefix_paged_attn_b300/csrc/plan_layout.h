@@ -36,12 +36,17 @@ struct Occ {
 };
 
 // A work item: one chunk, one KV head, and a row group = rows[row_off .. row_off + n_rows)
-// (row groups are shared by every KV head of a chunk).
+// (row groups are shared by every KV head of a chunk).  n_pages: the chunk's first pages that
+// the item reads -- all of them, unless no row of the group can see past some page (a row's
+// query token lies before the rest of the chunk: prefill-shaped plans, where every token of a
+// branch is a query); the kernels stop there.
 struct Item {
     int32_t chunk;
     int32_t head;
     int32_t row_off;
     int32_t n_rows;
+    int32_t n_pages;
+    int32_t pad[3];
 };
 
 // One stacked query row of a row group: a (reader, query token, query head in the GQA group).
@@ -71,13 +76,24 @@ struct Branch {
 
 // Per query token, what the merge kernel needs: its branch's partial-row bases
 // merge_bases[merge_off .. merge_off + n_merge), whether its only chunk wrote `out` directly,
-// and its index i among the branch's query tokens.
+// its index i among the branch's query tokens, and its logical position pos.  The first
+// kMergeInline bases, with the first logical position of each one's chunk, are also held
+// here, so that a token with that many partials or fewer needs one load of this record
+// before it loads the partials themselves.  The merge skips a partial whose chunk starts
+// after pos (merge_lpos, parallel to merge_bases): the token sees nothing of that chunk, and
+// the planner may have left the item that would have written the partial out.
+constexpr int kMergeInline = 5;
 struct QMerge {
     int32_t merge_off;
     int32_t n_merge;
     int32_t direct;
     int32_t i;
+    int32_t pos;
+    int32_t base[kMergeInline];
+    int32_t lpos[kMergeInline];
+    int32_t pad;
 };
+static_assert(sizeof(QMerge) == 64, "one 64-byte record per query token");
 
 // Byte offsets of the arrays inside the device plan buffer.  The first 256 bytes are a
 // header of int32 words, zero in the uploaded plan: [0] the device error word, [1] [2] the
@@ -85,7 +101,7 @@ struct QMerge {
 // to zero); the other words are unused and stay zero.
 struct Layout {
     int64_t chunk_pages, chunks, items_rows, items_tc, items_r8, rows, branches, q_merge, merge_bases,
-        mask_words, total;
+        merge_lpos, mask_words, total;
     int32_t n_chunk_pages, n_chunks, n_items_rows, n_items_tc, n_items_r8, n_rows, n_branches, total_q,
         n_merge_bases, n_mask_words;
 };

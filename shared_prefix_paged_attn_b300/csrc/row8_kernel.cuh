@@ -72,7 +72,8 @@ __global__ void __launch_bounds__(kThreads, 3) row8_kernel(const __grid_constant
     const int gid = lane >> 2, tig = lane & 3;
     const Item it = p.items_r8[blockIdx.x];
     ptx::launch_dependents();  // the next kernel of the decode may take the SMs this grid leaves
-    const Chunk ch = p.chunks[it.chunk];
+    Chunk ch = p.chunks[it.chunk];
+    ch.n_pages = it.n_pages;  // the pages this item reads (a prefix of the chunk)
     const int n_pages = ch.n_pages;
     const int32_t *pages = p.chunk_pages + ch.page_off;
 

@@ -263,7 +263,8 @@ __global__ void __launch_bounds__(kThreads, 2) row_kernel(const __grid_constant_
     const int gid = lane >> 2, tig = lane & 3;
     const Item it = p.items[blockIdx.x];
     ptx::launch_dependents();  // the next kernel of the decode may take the SMs this grid leaves
-    const Chunk ch = p.chunks[it.chunk];
+    Chunk ch = p.chunks[it.chunk];
+    ch.n_pages = it.n_pages;  // the pages this item reads (a prefix of the chunk)
 
     if (tid == 0) {
         for (int w = 0; w < kWarps; ++w)

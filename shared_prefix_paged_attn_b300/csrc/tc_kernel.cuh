@@ -479,7 +479,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
 
     auto item_ok = [&](int i) {  // items the planner never makes are refused, uniformly
         const Item it = p.items_tc[i];
-        return p.chunks[it.chunk].n_pages <= kMaxChunkPages && it.n_rows <= kRows;
+        return it.n_pages <= kMaxChunkPages && it.n_rows <= kRows;
     };
     // the next item this CTA runs (a refused item sets the error word and is skipped)
     auto next_item = [&]() {
@@ -516,7 +516,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
             const int i = sm.item;
             if (i >= p.n_items_tc) break;
             const Item it = p.items_tc[i];
-            const Chunk ch = p.chunks[it.chunk];
+            Chunk ch = p.chunks[it.chunk];
+            ch.n_pages = it.n_pages;  // the pages this item reads (a prefix of the chunk)
             const int T = (ch.n_pages + kTilePages - 1) / kTilePages;
             const int MT = it.n_rows > kTcRows ? 2 : 1;
             tc::fence_before();
@@ -564,7 +565,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
             const int i = sm.item;
             if (i >= p.n_items_tc) break;
             const Item it = p.items_tc[i];
-            const Chunk ch = p.chunks[it.chunk];
+            Chunk ch = p.chunks[it.chunk];
+            ch.n_pages = it.n_pages;  // the pages this item reads (a prefix of the chunk)
             const int T = (ch.n_pages + kTilePages - 1) / kTilePages;
             const int MT = it.n_rows > kTcRows ? 2 : 1;
             // the row's table entry, and its Q row -> shared memory, 128-byte swizzled K-major

@@ -321,14 +321,48 @@ def config5(shrink: int = 1, requests: int = 32, device="cpu", values=True) -> W
                    values=values)
 
 
+def packed_dag_prefill(shrink: int = 1, threads: int = 8, device="cpu", values=True) -> Workload:
+    """Packed DAG prefill of one episode: Hq 32 / Hkv 8, a root of 4K tokens, ``threads``
+    threads of U{1K..3K} tokens each; thread j >= 1 mounts the last 512 tokens of one random
+    earlier thread.  Every token is a query: the root's tokens see the root causally, a
+    thread's tokens see the root, its mount, and its own tokens causally (no drops).
+
+    Octopus (zicq.com), "Packed DAG-GRPO": all branches of an episode go through one
+    block-sparse attention whose mask holds intra-thread causality and the allowed
+    cross-thread reads; as a descriptor that is one branch per thread, listing the segments
+    it may read, with its own tokens as its queries."""
+    bld = _Builder(SEED_BASE + 6)
+    root = bld.new_segment(max(4096 // shrink, 1))
+    bld.add_branch([root], max(4096 // shrink, 1))
+    own = []
+    mount = max(512 // shrink, 1)
+    for j in range(threads):
+        ln = max(bld.randint(1024, 3072) // shrink, 1)
+        seg = bld.new_segment(ln)
+        lst = [root]
+        if j >= 1:
+            lst.append(bld.tail_view(own[bld.randint(0, j - 1)], mount))
+        own.append(seg)
+        bld.add_branch(lst + [seg], ln)
+    return _finish("packed_dag_prefill", 32, 8, bld, device=device, values=values)
+
+
 CONFIGS = {1: config1, 2: config2, 3: config3, 4: config4, 5: config5}
+PREFILL_SMALL = dict(shrink=16)
 
 # Shrink factors for the parity cases the oracle checks in full (seconds on a few cores).
 SMALL = {1: dict(shrink=1), 2: dict(shrink=8), 3: dict(shrink=16), 4: dict(shrink=16),
          5: dict(shrink=8, requests=4)}
 
 
+# Workload 6: the prefill-shaped one (every token a query), beside the five decodes.
+PREFILL = 6
+
+
 def make(config: int, small: bool = False, device: str = "cpu", values: bool = True) -> Workload:
+    if config == PREFILL:
+        kw = dict(PREFILL_SMALL) if small else {}
+        return packed_dag_prefill(device=device, values=values, **kw)
     kw = dict(SMALL[config]) if small else {}
     return CONFIGS[config](device=device, values=values, **kw)
 

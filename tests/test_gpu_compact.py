@@ -128,3 +128,77 @@ def test_decode_over_the_compacted_cache_matches_the_original():
     assert np.array_equal(np.isneginf(lse), ~fin)
     assert np.abs(out[fin] - ref_out[fin]).max() <= 1e-2
     assert np.abs(lse[fin] - ref_lse[fin]).max() <= 1e-3
+
+
+def _check_shared(w, branches, reposition, base=10000.0):
+    # share_prefix: the common prefix's kept entries packed once, then each branch's own;
+    # every branch, read through [shared pages][its own pages], holds exactly what the
+    # per-branch definition gives (so the rotation of a shared entry is the same for every
+    # reader: the common prefix starts at logical index 0)
+    dev = torch.device("cuda")
+    P, rs = C.common_prefix(w, branches)
+    want = [len(C.kept_indices(w, b)) for b in branches]
+    need = (rs + 15) // 16 + sum((r - rs + 15) // 16 for r in want)
+    pool = w.num_pages_pool
+    shape = (pool + need,) + tuple(w.k_pages.shape[1:])
+    filler = torch.Generator().manual_seed(10)
+    k = torch.randn(shape, generator=filler).to(torch.bfloat16)
+    v = torch.randn(shape, generator=filler).to(torch.bfloat16)
+    k[:pool], v[:pool] = w.k_pages, w.v_pages
+    k0, v0 = k.clone(), v.clone()
+    w2 = copy.copy(w)
+    w2.num_pages_pool = shape[0]
+    fresh = np.arange(pool, pool + need, dtype=np.int32)
+    plan = fa.fork_attn_compact_create(w2, branches, fresh, reposition=reposition, rope_base=base,
+                                       share_prefix=True)
+    assert plan.shared() == (rs, P)
+    kept, wb = plan.sizes()
+    assert kept.tolist() == want
+    kd, vd = k.to(dev), v.to(dev)
+    work = torch.empty(wb // 4 + 64, dtype=torch.int32, device=dev)
+    fa.fork_attn_compact_upload(plan, work)
+    fa.fork_attn_compact_run(plan, kd, vd)
+    torch.cuda.synchronize()
+    kd, vd = kd.cpu(), vd.cpu()
+    written = torch.zeros(kd.shape[0], kd.shape[2], dtype=torch.bool)
+    shared_pages = fresh[:(rs + 15) // 16].astype(np.int64)
+    at = len(shared_pages)
+    for b, r in zip(branches, want):
+        own = fresh[at:at + (r - rs + 15) // 16].astype(np.int64)
+        at += len(own)
+        n = np.arange(r)
+        pg = np.where(n < rs, shared_pages[np.minimum(n, max(rs - 1, 0)) // 16] if rs else 0,
+                      own[np.maximum(n - rs, 0) // 16] if len(own) else 0)
+        sl = np.where(n < rs, n % 16, (n - rs) % 16)
+        pg, sl = torch.as_tensor(pg), torch.as_tensor(sl)
+        written[pg, sl] = True
+        K, V, _ = C.compact(w, b, reposition=reposition, base=base)
+        assert np.array_equal(vd[pg, :, sl, :].double().numpy(), V)
+        got_k = kd[pg, :, sl, :].double().numpy()
+        if not reposition:
+            assert np.array_equal(got_k, K)
+        else:
+            ulp = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(K), 1e-30))) - 7)
+            src = C.compact(w, b)[0]
+            pair = np.abs(src[..., :64]) + np.abs(src[..., 64:])
+            opnd = np.concatenate([pair, pair], axis=-1)
+            assert np.all(np.abs(got_k - K) <= 0.5 * ulp + 1e-6 * opnd + 1e-9)
+    assert at == need
+    keep = ~written
+    assert torch.equal(kd.transpose(1, 2)[keep], k0.transpose(1, 2)[keep])
+    assert torch.equal(vd.transpose(1, 2)[keep], v0.transpose(1, 2)[keep])
+
+
+@pytest.mark.parametrize("cfg", [1, 2, 4])
+@pytest.mark.parametrize("reposition", [False, True])
+def test_shared_prefix_mode(cfg, reposition):
+    w = W.make(cfg, small=True)
+    _check_shared(w, list(range(min(w.num_branches, 6))), reposition)
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_shared_prefix_mode_random_caches(seed):
+    # random caches: the common prefix is often empty or a single segment
+    w = W.random_dag(700 + seed, n_branches=4, n_segs=4, max_seg_len=200, pool_pages=50,
+                     drop_p=(0.0, 0.3)[seed % 2])
+    _check_shared(w, list(range(w.num_branches)), seed >= 2)

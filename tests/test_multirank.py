@@ -57,3 +57,92 @@ def test_ranks_solve_independent_problems_of_the_same_shape(two_ranks):
     assert int(a["seed"]) != int(b["seed"])
     assert int(a["unique"]) == int(b["unique"])  # same structure, so the same unique KV bytes
     assert not np.array_equal(a["q"], b["q"])    # different values
+
+
+def _split_main(rank, world, port, out_dir):
+    # one problem split over the ranks (by KV head, then by request); each rank runs the
+    # oracle on its share and rank 0 puts the shares back together
+    os.environ.update(WORLD_SIZE=str(world), RANK=str(rank), LOCAL_RANK=str(rank),
+                      MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    sys.path.insert(0, ROOT)
+    import torch.distributed as dist
+    import oracle
+    from shared_prefix_paged_attn_b300 import shard
+    from shared_prefix_paged_attn_b300 import workloads as W
+    dist.init_process_group("gloo")
+    w = W.make(5, small=True)
+    threads = max(1, oracle.threads_default() // world)
+    res = {}
+    sub = shard.split_by_kv_head(w, rank, world)
+    o, l = oracle.fork_attn(sub, threads=threads)
+    got = [None] * world
+    dist.all_gather_object(got, (o.reshape(sub.total_q, sub.num_q_heads, -1),
+                                 l.reshape(sub.total_q, sub.num_q_heads)))
+    res["head"] = got
+    sub, mine = shard.split_by_request(w, rank, world)
+    o, l = oracle.fork_attn(sub, threads=threads)
+    got = [None] * world
+    dist.all_gather_object(got, (mine, o.reshape(sub.total_q, sub.num_q_heads, -1),
+                                 l.reshape(sub.total_q, sub.num_q_heads),
+                                 oracle.unique_slots(sub)[0]))
+    res["request"] = got
+    if rank == 0:
+        import pickle
+        with open(os.path.join(out_dir, "split.pkl"), "wb") as f:
+            pickle.dump(res, f)
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+@pytest.fixture(scope="module")
+def split_ranks(tmp_path_factory):
+    out = tmp_path_factory.mktemp("split")
+    mp.start_processes(_split_main, args=(2, _free_port(), str(out)), nprocs=2, join=True,
+                       start_method="spawn")
+    import pickle
+    with open(out / "split.pkl", "rb") as f:
+        return pickle.load(f)
+
+
+def test_split_by_kv_head_concatenates_to_the_whole_problem_bitwise(split_ranks):
+    import oracle
+    from shared_prefix_paged_attn_b300 import shard
+    from shared_prefix_paged_attn_b300 import workloads as W
+    w = W.make(5, small=True)
+    ref_o, ref_l = oracle.fork_attn(w)
+    parts = split_ranks["head"]
+    assert [p[1].shape[1] for p in parts] == [16, 16]
+    o = shard.gather_heads([torch.from_numpy(p[0]) for p in parts], w).numpy()
+    l = shard.gather_heads([torch.from_numpy(p[1]) for p in parts], w).numpy()
+    assert np.array_equal(o.reshape(-1, 128), ref_o) and np.array_equal(l.reshape(-1), ref_l)
+
+
+def test_split_by_request_concatenates_to_the_whole_problem_bitwise(split_ranks):
+    import oracle
+    from shared_prefix_paged_attn_b300 import shard
+    from shared_prefix_paged_attn_b300 import workloads as W
+    w = W.make(5, small=True)
+    ref_o, ref_l = oracle.fork_attn(w)
+    parts = split_ranks["request"]
+    mine = [p[0] for p in parts]
+    assert sorted(mine[0] + mine[1]) == list(range(w.num_branches))
+    assert len(mine[0]) == len(mine[1]) == 16  # 4 requests of 8 branches: two on each rank
+    o = shard.gather_rows([torch.from_numpy(p[1]) for p in parts], mine, w).numpy()
+    l = shard.gather_rows([torch.from_numpy(p[2]) for p in parts], mine, w).numpy()
+    assert np.array_equal(o.reshape(-1, 128), ref_o) and np.array_equal(l.reshape(-1), ref_l)
+    # no page is read by both ranks: the shares' unique KV adds up to the whole problem's
+    assert parts[0][3] + parts[1][3] == oracle.unique_slots(w)[0]
+
+
+def test_request_groups_follow_shared_pages():
+    from shared_prefix_paged_attn_b300 import shard
+    from shared_prefix_paged_attn_b300 import workloads as W
+    assert shard.request_groups(W.make(5, small=True, values=False)) == [list(range(8 * i, 8 * i + 8)) for i in range(4)]
+    # one shared prefix (and mounts across leaves) make one request
+    for cfg in (2, 3, 4):
+        assert len(shard.request_groups(W.make(cfg, small=True, values=False))) == 1
+    with pytest.raises(ValueError):
+        shard.request_assignment(W.make(2, small=True, values=False), 2)
+    assert shard.head_range(8, 0, 3) == (0, 3) and shard.head_range(8, 2, 3) == (6, 8)
+    with pytest.raises(ValueError):
+        shard.head_range(2, 0, 4)

@@ -239,3 +239,39 @@ def test_prefill_shaped_descriptors_plan_like_decodes(seed):
     w.branch_q_off[1:] += 1
     with pytest.raises(fa.ForkAttnError):
         fa.plan_for(w)
+
+
+def test_packed_dag_prefill_workload_structure():
+    # one branch per thread: the root's tokens query the root; thread j's tokens query the
+    # root, one mounted terminal block of an earlier thread (j >= 1), and its own segment
+    w = W.packed_dag_prefill(shrink=16, values=False)
+    assert w.num_branches == 9
+    root = int(w.branch_segs[w.branch_seg_off[0]])
+    assert w.branch_len(0) == int(w.branch_q_off[1]) == 256
+    for b in range(1, w.num_branches):
+        lst = w.branch_segs[w.branch_seg_off[b]:w.branch_seg_off[b + 1]]
+        assert int(lst[0]) == root and len(lst) == (2 if b == 1 else 3)
+        own = int(lst[-1])
+        assert int(w.branch_q_off[b + 1] - w.branch_q_off[b]) == int(w.segs[own][2])
+        if b >= 2:  # the mount reads the last 32 tokens of an earlier thread's pages in place
+            m = w.segs[int(lst[1])]
+            assert int(m[2]) == 32
+            slots = set(W.logical_slots(w, b)[256:256 + 32].tolist())
+            assert any(slots <= set(W.logical_slots(w, a)[-32:].tolist()) for a in range(1, b))
+
+
+@pytest.mark.parametrize("chunk_pages", [0, 3])
+def test_packed_dag_prefill_plan(chunk_pages):
+    # causally visible pairs only; with short chunks whole (row group, chunk) pairs are left
+    # out (every row of the group lies before the chunk), with one chunk per run none are
+    w = W.packed_dag_prefill(shrink=16, values=False)
+    st = fa.plan_for(w, chunk_pages=chunk_pages).stats()
+    G = w.num_q_heads // w.num_kv_heads
+    want = sum(_visible_pairs(w, b) for b in range(w.num_branches)) * G * w.num_kv_heads * 4 * 128
+    assert st["flops_rows"] + st["flops_tensor"] == want
+    assert st["total_q"] == w.total_q
+    assert (st["unique_visible_slots"], st["touched_pages"]) == oracle.unique_slots(w)
+    if chunk_pages:
+        assert st["items_skipped"] > 0
+    full = fa.plan_for(W.packed_dag_prefill(values=False)).stats()
+    assert full["num_items_tensor"] > 0 and full["num_items_rows"] == 0
