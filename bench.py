@@ -428,6 +428,63 @@ def measure_config(cfg, args, dev, flush, dist, rank, world, steps, keep=False):
     return res
 
 
+def measure_scoring(args, dev, flush, steps):
+    """Key scoring by 32 representative queries of each of the first 8 branches of the
+    long-context rolling-drop workload, then a keep of a quarter of each branch's visible
+    entries: pass 1 (the decode on the representatives plan, for lse), pass 2 (the tcgen05
+    scoring kernel + head reduce) and the top-k, each timed with CUDA events on the stream."""
+    w = W.make(4, device=str(dev))
+    ws = W.with_representatives(w, list(range(8)), reps=32, device=str(dev))
+    del w
+    sc = fa.KeyScorer(ws, device=dev)
+    st = sc.plan.stats()
+    n_vis = []
+    for b in range(ws.num_branches):
+        words = ws.vis_bits[ws.vis_word_off[b]:ws.vis_word_off[b + 1]]
+        bits = np.unpackbits(words.view(np.uint8), bitorder="little")[:ws.branch_len(b)]
+        n_vis.append(int(bits.sum()))
+    keep_k = torch.as_tensor(np.array([n // 4 for n in n_vis], np.int32), device=dev)
+    stream = torch.cuda.current_stream(dev)
+    q, k, v = ws.q, ws.k_pages, ws.v_pages
+    for _ in range(args.warmup):
+        flush.zero_()
+        sc.score(q, k, v, stream)
+        sc.topk(keep_k, stream)
+    torch.cuda.synchronize(dev)
+    assert fa.fork_attn_check(sc.plan, stream) == 0
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+        for i in range(steps):
+            flush.zero_()
+            ev[i][0].record(stream)
+            fa.fork_attn_decode(q, k, v, sc.plan, sc.out, sc.lse, stream)
+            ev[i][1].record(stream)
+            fa.fork_attn_score(q, k, sc.plan, sc.lse, sc.scores, stream)
+            ev[i][2].record(stream)
+            sc.topk(keep_k, stream)
+            ev[i][3].record(stream)
+        torch.cuda.synchronize(dev)
+    assert fa.fork_attn_check(sc.plan, stream) == 0
+    t = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(3)] for e in ev])  # ms
+    ms = t.mean(axis=0)
+    step = float(t.sum(axis=1).mean())
+    keys = sum(n_vis)
+    flops2 = keys * ws.meta["reps"] * ws.num_q_heads * 2 * 128  # QK^T of pass 2 (visible keys)
+    tpk, tpk_kind = tensor_peak()
+    return {"workload": ws.name, "branches": ws.num_branches, "reps": ws.meta["reps"],
+            "Hq": ws.num_q_heads, "Hkv": ws.num_kv_heads, "visible_keys": keys,
+            "metric": "keys scored and kept per second (both passes + top-k)",
+            "value": keys / (step * 1e-3), "unit": "keys/s", "ms_per_step": step,
+            "ms_lse_pass": float(ms[0]), "ms_score_pass": float(ms[1]), "ms_topk": float(ms[2]),
+            "score_pass": {"bound": "tensor", "achieved": flops2 / (ms[1] * 1e-3) / 1e12,
+                           "unit": "TFLOP/s", "peak": tpk, "peak_kind": tpk_kind,
+                           "frac": flops2 / (ms[1] * 1e-3) / 1e12 / tpk, "algorithmic": flops2,
+                           "exp_per_s": keys * ws.meta["reps"] * ws.num_q_heads / (ms[1] * 1e-3)},
+            "lse_pass_tflops": (st["flops_rows"] + st["flops_tensor"]) / (ms[0] * 1e-3) / 1e12,
+            "keep": "a quarter of each branch's visible entries", "steps": steps,
+            "clocks": clk.record(), "gpu_launches": steps * 6}
+
+
 def run_ours(args):
     dist, rank, world, local = dist_setup(args.gpus)
     dev = torch.device("cuda", local if world > 1 else 0)
@@ -537,6 +594,10 @@ def run_ours(args):
                    "tensor_ctas": rs["tensor_ctas"], "clocks": r["clocks"],
                    "steps": max(3, min(K, 20)), "gpu_launches": max(3, min(K, 20)) * r["launches_per_step"]}
 
+    scoring = None
+    if not args.no_scoring and rank == 0 and world == 1:
+        scoring = measure_scoring(args, dev, flush, max(3, min(K, 20)))
+
     if rank == 0:
         line = {
             "metric": METRIC, "value": head["value"], "unit": "GB/s", "n_gpus": world, "steps": K,
@@ -563,6 +624,7 @@ def run_ours(args):
             "cpu_baseline": cpu,
             "per_config": per_config,
             "packed_dag_prefill": prefill,
+            "key_scoring": scoring,
             "gpu": torch.cuda.get_device_name(dev),
         }
         print(json.dumps(line), flush=True)
@@ -646,6 +708,8 @@ def main():
     ap.add_argument("--split", choices=["none", "head", "request"], default="none",
                     help="with N > 1: every rank its own problem (none, weak scaling) or a share "
                          "of one problem by KV head or by request (strong scaling)")
+    ap.add_argument("--no-scoring", action="store_true",
+                    help="leave out the key-scoring entry of the line")
     ap.add_argument("--no-prefill", action="store_true",
                     help="leave out the packed DAG prefill entry of the line")
     ap.add_argument("--compact", action="store_true",

@@ -121,7 +121,11 @@ typedef struct {
                             /* split of SMs between it and the row kernels)                  */
     int32_t tensor_chunk_pages; /* max pages per tcgen05 chunk, rounded up to whole 8-page   */
                             /* tiles (0 = chosen by the planner)                             */
-    int32_t reserved[3];    /* must be 0                                                     */
+    int32_t representatives;/* 1: the query tokens are representative queries for key       */
+                            /* scoring: each sees its branch's whole visible list (no causal */
+                            /* limit; n_q may exceed n_b), and the plan can also drive       */
+                            /* fork_attn_score / fork_attn_topk.  0: decode queries          */
+    int32_t reserved[2];    /* must be 0                                                     */
 } fa_plan_opts;
 
 /* Counters of a plan, for measurement.  unique_visible_slots: distinct physical token slots
@@ -328,6 +332,38 @@ int fork_attn_compact_run(const fa_compact *c, void *k_pages, void *v_pages, voi
 
 /* Frees the compaction plan (not the caller's device buffers). */
 int fork_attn_compact_destroy(fa_compact *c);
+
+/* ---- Key scoring by representative queries, and top-k keep ----
+ * AgentKV blog (rit.work), "Как AgentKV выбирает и освобождает записи кэша": the recent
+ * queries of every phase are merged into one set of representatives (32 in the main
+ * experiments), every key is scored by the mean attention the representatives give it, and
+ * the entries with the largest scores are kept.  For branch b of a plan made with
+ * fa_plan_opts.representatives = 1, its n_q query tokens are its representatives r < R, and
+ * for each of its visible entries j
+ *     score(j) = 1 / (R Hq) * sum over r < R, h < Hq of exp(s_{r,h,j} - lse_{r,h}),
+ * s_{r,h,j} = scale <q_{r,h}, K[slot(j), h / G]>, lse_{r,h} over the branch's visible entries
+ * (no causal limit).  Three calls on one stream:
+ *   1. fork_attn_decode(q, k, v, plan, out, lse, stream): the lse of every representative row
+ *      (out is computed too and may be ignored);
+ *   2. fork_attn_score(q, k, plan, lse, scores, stream): scores [device, fp32,
+ *      total_entries]: branch b's entries at entry_off[b] + j, entry_off the running sum of
+ *      the branches' list lengths n_b; an entry the branch does not see is NaN.  Uses the
+ *      plan's scratch (per-KV-head scores) and sets the plan's error word (fork_attn_check);
+ *   3. fork_attn_topk(plan, scores, keep_k, keep_bits, stream): keep_k [device, int32,
+ *      num_branches]; keep_bits [device, uint32, total_words]: branch b's new visibility bits,
+ *      bit j % 32 of word word_off[b] + j / 32 (word_off the running sum of ceil(n_b / 32)),
+ *      set for the k_b visible entries with the largest scores, equal scores keeping the
+ *      smaller j (all visible entries when k_b >= their number, none when k_b <= 0).
+ * q, k_pages, lse: as fork_attn_decode's (16-byte aligned), the same plan, uploaded.  Errors:
+ * FA_ERR_NULL, FA_ERR_INVALID (not a representatives plan), FA_ERR_NOT_UPLOADED,
+ * FA_ERR_ALIGN, FA_ERR_CUDA.  fork_attn_plan_create refuses a representatives plan with
+ * n_q x G > 256 for a branch (FA_ERR_UNSUPPORTED). */
+int fork_attn_score(const void *q, const void *k_pages, const fa_plan *plan, const float *lse,
+                    float *scores, void *stream);
+int fork_attn_topk(const fa_plan *plan, const float *scores, const int32_t *keep_k,
+                   uint32_t *keep_bits, void *stream);
+/* total_entries / total_words (either may be NULL): the sizes of scores and keep_bits. */
+int fork_attn_score_sizes(const fa_plan *plan, int64_t *total_entries, int64_t *total_words);
 
 /* Frees the host plan.  Device buffers stay owned by the caller. */
 int fork_attn_plan_destroy(fa_plan *plan);

@@ -14,8 +14,9 @@ from . import _lib
 from ._lib import FA_BF16, FA_F32, FaCompactDims, FaDesc, FaDims, FaPlanOpts, FaPlanStats
 
 __all__ = ["ForkAttnError", "Plan", "fork_attn_plan_create", "fork_attn_decode",
-           "fork_attn_decode_timed", "fork_attn_decode_static_scratch", "fork_attn_check", "fork_attn_strerror", "FA_BF16",
-           "FA_F32", "plan_for", "ForkAttention", "CompactPlan", "fork_attn_compact_create", "fork_attn_compact_upload", "fork_attn_compact_run"]
+           "fork_attn_decode_timed", "fork_attn_decode_static_scratch", "fork_attn_score",
+           "fork_attn_topk", "fork_attn_score_sizes", "KeyScorer", "fork_attn_check",
+           "fork_attn_strerror", "FA_BF16", "FA_F32", "plan_for", "ForkAttention", "CompactPlan", "fork_attn_compact_create", "fork_attn_compact_upload", "fork_attn_compact_run"]
 
 
 class ForkAttnError(RuntimeError):
@@ -106,7 +107,7 @@ def fork_attn_plan_create(num_q_heads, num_kv_heads, page_ids, segs, branch_seg_
                           branch_segs, num_pages_pool, branch_q_off=None, vis_bits=None,
                           vis_word_off=None, scale=None, out_dtype=FA_BF16, head_dim=128,
                           page_size=16, chunk_pages=0, num_sms=0, tensor_min_rows=0,
-                          tensor_ctas=0, tensor_chunk_pages=0) -> Plan:
+                          tensor_ctas=0, tensor_chunk_pages=0, representatives=0) -> Plan:
     """fork_attn_plan_create over host (numpy) descriptor arrays."""
     keep = []
 
@@ -124,6 +125,7 @@ def fork_attn_plan_create(num_q_heads, num_kv_heads, page_ids, segs, branch_seg_
     opts = FaPlanOpts()
     opts.chunk_pages, opts.num_sms, opts.tensor_min_rows = int(chunk_pages), int(num_sms), int(tensor_min_rows)
     opts.tensor_ctas, opts.tensor_chunk_pages = int(tensor_ctas), int(tensor_chunk_pages)
+    opts.representatives = int(representatives)
     handle = ctypes.c_void_p()
     _check(_lib.load().fork_attn_plan_create(ctypes.byref(dims), ctypes.byref(desc),
                                              ctypes.byref(opts), ctypes.byref(handle)),
@@ -159,6 +161,53 @@ def fork_attn_decode_static_scratch(q, k_pages, v_pages, plan: Plan, out, lse, s
                                                        plan.handle, _ptr(out), _ptr(lse),
                                                        _stream_ptr(stream)),
            "fork_attn_decode_static_scratch")
+
+
+def fork_attn_score(q, k_pages, plan: Plan, lse, scores, stream=None):
+    """fork_attn_score: scores [device fp32, total_entries] of every branch's entries."""
+    _check(_lib.load().fork_attn_score(_ptr(q), _ptr(k_pages), plan.handle, _ptr(lse), _ptr(scores),
+                                       _stream_ptr(stream)), "fork_attn_score")
+
+
+def fork_attn_topk(plan: Plan, scores, keep_k, keep_bits, stream=None):
+    """fork_attn_topk: keep_k [device int32, B]; keep_bits [device int32/uint32, total_words]."""
+    _check(_lib.load().fork_attn_topk(plan.handle, _ptr(scores), _ptr(keep_k), _ptr(keep_bits),
+                                      _stream_ptr(stream)), "fork_attn_topk")
+
+
+def fork_attn_score_sizes(plan: Plan):
+    """(total_entries, total_words) of a representatives plan."""
+    e, wds = ctypes.c_int64(), ctypes.c_int64()
+    _check(_lib.load().fork_attn_score_sizes(plan.handle, ctypes.byref(e), ctypes.byref(wds)),
+           "fork_attn_score_sizes")
+    return e.value, wds.value
+
+
+class KeyScorer:
+    """Representative-query scoring of a workload whose query tokens are the representatives
+    (plan, buffers, and the three calls: decode for lse, score, top-k)."""
+
+    def __init__(self, w, device="cuda", stream=None, **opts):
+        import torch
+        self.plan = plan_for(w, out_dtype=FA_F32, representatives=1, **opts)
+        pb, sb = self.plan.sizes()
+        self.plan_buf = torch.empty(pb, dtype=torch.uint8, device=device)
+        self.scratch = torch.empty(max(sb, 1), dtype=torch.uint8, device=device)
+        self.plan.upload(self.plan_buf, self.scratch, stream)
+        E, nw = fork_attn_score_sizes(self.plan)
+        self.out = torch.empty((w.total_q, w.num_q_heads, w.head_dim), dtype=torch.float32, device=device)
+        self.lse = torch.empty((w.total_q, w.num_q_heads), dtype=torch.float32, device=device)
+        self.scores = torch.empty(max(E, 1), dtype=torch.float32, device=device)
+        self.keep_bits = torch.empty(max(nw, 1), dtype=torch.int32, device=device)
+
+    def score(self, q, k_pages, v_pages, stream=None):
+        fork_attn_decode(q, k_pages, v_pages, self.plan, self.out, self.lse, stream)
+        fork_attn_score(q, k_pages, self.plan, self.lse, self.scores, stream)
+        return self.scores
+
+    def topk(self, keep_k, stream=None):
+        fork_attn_topk(self.plan, self.scores, keep_k, self.keep_bits, stream)
+        return self.keep_bits
 
 
 def fork_attn_check(plan: Plan, stream=None) -> int:

@@ -34,7 +34,7 @@ class FaDesc(ctypes.Structure):
 class FaPlanOpts(ctypes.Structure):
     _fields_ = [("chunk_pages", c_int32), ("num_sms", c_int32), ("tensor_min_rows", c_int32),
                 ("tensor_ctas", c_int32), ("tensor_chunk_pages", c_int32),
-                ("reserved", c_int32 * 3)]
+                ("representatives", c_int32), ("reserved", c_int32 * 2)]
 
 
 class FaPlanStats(ctypes.Structure):
@@ -78,6 +78,9 @@ SIGNATURES = {
                                            ctypes.POINTER(c_void_p)]),
     "fork_attn_compact_sizes": (c_int32, [c_void_p, c_void_p, ctypes.POINTER(ctypes.c_size_t)]),
     "fork_attn_compact_shared": (c_int32, [c_void_p, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int64)]),
+    "fork_attn_score": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
+    "fork_attn_topk": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
+    "fork_attn_score_sizes": (c_int32, [c_void_p, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int64)]),
     "fork_attn_compact_upload": (c_int32, [c_void_p, c_void_p, ctypes.c_size_t, c_void_p]),
     "fork_attn_compact_run": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p]),
     "fork_attn_compact_destroy": (c_int32, [c_void_p]),

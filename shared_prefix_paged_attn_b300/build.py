@@ -6,7 +6,7 @@ import sys
 HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libforkattn.so")
-SOURCES = ["plan.cpp", "decode.cu", "compact.cu"]
+SOURCES = ["plan.cpp", "decode.cu", "compact.cu", "score.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -53,6 +53,12 @@ struct Input {
     int32_t G;
     std::vector<int64_t> n_b;
     std::vector<int32_t> q_off;
+    bool reps = false;  // representative queries: each sees its branch's whole list
+    // logical position of branch b's query token i: the last n_q positions of the branch, or,
+    // for representative queries, past the end of the list (no causal limit)
+    int64_t qpos(int32_t b, int64_t i) const {
+        return reps ? n_b[b] - 1 : n_b[b] - (q_off[b + 1] - q_off[b]) + i;
+    }
 };
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -102,7 +108,8 @@ int validate(Input &in) {
     for (int32_t b = 0; b < B; ++b) {
         const int64_t nq = s->branch_q_off ? int64_t(s->branch_q_off[b + 1]) - s->branch_q_off[b] : 1;
         if (s->branch_q_off && s->branch_q_off[0] != 0) return FA_ERR_INVALID;
-        if (nq < 1 || nq > in.n_b[b]) return FA_ERR_INVALID;
+        if (nq < 1 || (!in.reps && nq > in.n_b[b])) return FA_ERR_INVALID;
+        if (in.reps && nq * in.G > 2 * fa::kTcRows) return FA_ERR_UNSUPPORTED;
         in.q_off[b + 1] = int32_t(in.q_off[b] + nq);
         if (int64_t(in.q_off[b]) + nq > (int64_t(1) << 30)) return FA_ERR_INVALID;
     }
@@ -199,10 +206,10 @@ struct Builder {
     // Every reader of page group g sees all of the page before its branch's first query token:
     // no causal cut can fall inside it.
     bool pre_query(int32_t g) const {
+        if (in.reps) return true;  // no causal limit at all
         for (int32_t t = 0; t < group_count[g]; ++t) {
             const Rec &a = recs[by_page[group_start[g] + t]];
-            const int64_t qpos0 = in.n_b[a.branch] - (in.q_off[a.branch + 1] - in.q_off[a.branch]);
-            if (int64_t(a.lpos0) + kPageSize > qpos0) return false;
+            if (int64_t(a.lpos0) + kPageSize > in.qpos(a.branch, 0)) return false;
         }
         return true;
     }
@@ -274,6 +281,9 @@ struct Emit {
     std::vector<fa::QMerge> q_merge;
     std::vector<int32_t> merge_bases;
     std::vector<int32_t> merge_lpos;  // first logical position of each partial's chunk
+    // representative queries only (key scoring)
+    std::vector<fa::Item> score_items;
+    std::vector<int32_t> score_units, occ_pos, row_pos, entry_off, word_off;  // units: (item, tile0, tiles, 0)
     std::vector<uint32_t> mask_words;
 };
 
@@ -289,7 +299,10 @@ int build_plan(Input &in, const fa_plan_opts &opts, fa_plan *plan) {
     fa_plan_stats &st = plan->stats;
     std::memset(&st, 0, sizeof st);
 
-    const int32_t tmin = opts.tensor_min_rows < 0 ? 0 : (opts.tensor_min_rows > 0 ? opts.tensor_min_rows : 64);
+    // representative queries: every run on the tcgen05 kernel, so that a branch's rows of one
+    // chunk (n_q x G <= 256) always sit in one row group, which the scoring pass needs
+    const int32_t tmin = in.reps ? 1
+                                 : opts.tensor_min_rows < 0 ? 0 : (opts.tensor_min_rows > 0 ? opts.tensor_min_rows : 64);
     auto run_rows = [&](const std::vector<int32_t> &run) {  // stacked rows of a run's readers
         const int32_t g0 = run[0];
         int64_t rows = 0;
@@ -325,6 +338,21 @@ int build_plan(Input &in, const fa_plan_opts &opts, fa_plan *plan) {
             }
         }
     }
+    // key scoring: branch b's entries are scores[entry_off[b] .. + n_b), its keep bits the
+    // words word_off[b] .. + ceil(n_b / 32)
+    if (in.reps) {
+        int64_t e = 0, wsum = 0;
+        for (int32_t b = 0; b < B; ++b) {
+            em.entry_off.push_back(int32_t(e));
+            em.word_off.push_back(int32_t(wsum));
+            e += in.n_b[b];
+            wsum += ceil_div(in.n_b[b], 32);
+            if (e > (int64_t(1) << 31) - 1 || e * Hkv > (int64_t(1) << 40)) return FA_ERR_UNSUPPORTED;
+        }
+        em.entry_off.push_back(int32_t(e));
+        em.word_off.push_back(int32_t(wsum));
+    }
+
     std::vector<char> chunk_tc;  // per chunk: its items go to the tcgen05 kernel
     std::vector<int64_t> chunk_slots;  // per chunk: visible slots of its pages (any reader)
     std::vector<int32_t> occ_count(B, 0);
@@ -367,8 +395,8 @@ int build_plan(Input &in, const fa_plan_opts &opts, fa_plan *plan) {
                     // at or before the query token's position); query tokens from the first
                     // one whose position is past the page's last slot see all of its slots
                     const int64_t nq = in.q_off[rd.branch + 1] - in.q_off[rd.branch];
-                    const int64_t qpos0 = in.n_b[rd.branch] - nq;
-                    const int64_t i_full = std::min<int64_t>(nq, std::max<int64_t>(0, int64_t(rd.lpos0) + kPageSize - 1 - qpos0));
+                    const int64_t qpos0 = in.qpos(rd.branch, 0);
+                    const int64_t i_full = in.reps ? 0 : std::min<int64_t>(nq, std::max<int64_t>(0, int64_t(rd.lpos0) + kPageSize - 1 - qpos0));
                     int64_t pairs = (nq - i_full) * __builtin_popcount(rd.vis);
                     for (int64_t i = std::max<int64_t>(0, int64_t(rd.lpos0) - qpos0); i < i_full; ++i) {
                         const int64_t cut = qpos0 + i - rd.lpos0;  // slots s <= cut are causally visible
@@ -395,6 +423,15 @@ int build_plan(Input &in, const fa_plan_opts &opts, fa_plan *plan) {
                         if (k + 1 < len) w |= bd.recs[bd.by_page[bd.group_start[run[pos + k + 1]] + t]].vis << 16;
                         em.mask_words.push_back(w);
                     }
+                }
+                oc.pos_off = -1;
+                if (in.reps) {  // every page's slot-0 score index for this reader
+                    oc.pos_off = int32_t(em.occ_pos.size());
+                    for (int64_t k = 0; k < len; ++k) {
+                        const Rec &rk = bd.recs[bd.by_page[bd.group_start[run[pos + k]] + t]];
+                        em.occ_pos.push_back(int32_t(em.entry_off[rk.branch] + rk.lpos0));
+                    }
+                    if (em.occ_pos.size() > size_t(INT32_MAX)) return FA_ERR_UNSUPPORTED;
                 }
                 em.occs.push_back(oc);
                 occ_count[rd.branch] += 1;
@@ -427,7 +464,7 @@ int build_plan(Input &in, const fa_plan_opts &opts, fa_plan *plan) {
         std::memset(&br, 0, sizeof br);
         br.q_begin = in.q_off[b];
         br.n_q = in.q_off[b + 1] - in.q_off[b];
-        br.qpos0 = int32_t(in.n_b[b] - br.n_q);
+        br.qpos0 = int32_t(in.qpos(b, 0));
         br.merge_off = int32_t(em.merge_bases.size());
         br.n_merge = int32_t(per_branch[b].size());
         br.direct = occ_count[b] == 1;
@@ -440,7 +477,7 @@ int build_plan(Input &in, const fa_plan_opts &opts, fa_plan *plan) {
             qm.n_merge = br.n_merge;
             qm.direct = br.direct;
             qm.i = i;
-            qm.pos = br.qpos0 + i;
+            qm.pos = int32_t(in.qpos(b, i));
             for (int32_t k = 0; k < std::min(br.n_merge, fa::kMergeInline); ++k) {
                 qm.base[k] = per_branch[b][k];
                 qm.lpos[k] = per_branch_lpos[b][k];
@@ -474,10 +511,11 @@ int build_plan(Input &in, const fa_plan_opts &opts, fa_plan *plan) {
                     for (int32_t jh = 0; jh < G; ++jh) {
                         fa::RowRec r;
                         r.qrow0 = (br.q_begin + i) * Hq + jh;
-                        r.climit = br.qpos0 + i - oc.lpos0;
+                        r.climit = int32_t(in.qpos(oc.branch, i) - oc.lpos0);
                         r.mask_off = oc.mask_off;
                         r.prow0 = oc.prow_base < 0 ? -1 : oc.prow_base + (i * G + jh) * Hkv;
                         em.rows.push_back(r);
+                        if (in.reps) em.row_pos.push_back(oc.pos_off);
                     }
                 cur_rows += ni * G;
             }
@@ -532,6 +570,20 @@ int build_plan(Input &in, const fa_plan_opts &opts, fa_plan *plan) {
     std::stable_sort(em.items_tc.begin(), em.items_tc.end(), by_len);
     std::stable_sort(em.items_rows.begin(), em.items_rows.end(), by_len);
     std::stable_sort(em.items_r8.begin(), em.items_r8.end(), by_len);
+    if (in.reps) {  // the scoring pass takes every item, in units of <= 16 128-key tiles
+        for (const auto *list : {&em.items_tc, &em.items_rows, &em.items_r8})
+            em.score_items.insert(em.score_items.end(), list->begin(), list->end());
+        for (size_t i = 0; i < em.score_items.size(); ++i) {
+            const int32_t tiles = int32_t(ceil_div(em.score_items[i].n_pages, 8));
+            for (int32_t t0 = 0; t0 < tiles; t0 += fa::kScoreUnitTiles) {
+                em.score_units.push_back(int32_t(i));
+                em.score_units.push_back(t0);
+                em.score_units.push_back(std::min(fa::kScoreUnitTiles, tiles - t0));
+                em.score_units.push_back(0);
+            }
+            if (em.score_units.size() > size_t(INT32_MAX)) return FA_ERR_UNSUPPORTED;
+        }
+    }
 
     // Persistent CTAs of the tcgen05 kernel: the SMs it holds while the row kernels stream
     // the private runs on the others (and on each SM a tcgen05 CTA leaves once the work
@@ -620,7 +672,17 @@ int build_plan(Input &in, const fa_plan_opts &opts, fa_plan *plan) {
     L.merge_bases = place(int64_t(em.merge_bases.size()) * 4);
     L.merge_lpos = place(int64_t(em.merge_lpos.size()) * 4);
     L.mask_words = place(int64_t(em.mask_words.size()) * 4);
+    L.score_items = place(int64_t(em.score_items.size()) * sizeof(fa::Item));
+    L.score_units = place(int64_t(em.score_units.size()) * 4);
+    L.occ_pos = place(int64_t(em.occ_pos.size()) * 4);
+    L.row_pos = place(int64_t(em.row_pos.size()) * 4);
+    L.entry_off = place(int64_t(em.entry_off.size()) * 4);
+    L.word_off = place(int64_t(em.word_off.size()) * 4);
     L.total = off;
+    L.n_score_items = int32_t(em.score_items.size());
+    L.n_score_units = int32_t(em.score_units.size() / 4);
+    L.total_entries = em.entry_off.empty() ? 0 : em.entry_off.back();
+    L.total_words = em.word_off.empty() ? 0 : em.word_off.back();
     L.n_chunk_pages = int32_t(em.chunk_pages.size());
     L.n_chunks = int32_t(em.chunks.size());
     L.n_items_rows = int32_t(em.items_rows.size());
@@ -644,7 +706,14 @@ int build_plan(Input &in, const fa_plan_opts &opts, fa_plan *plan) {
     put(L.merge_bases, em.merge_bases.data(), em.merge_bases.size() * 4);
     put(L.merge_lpos, em.merge_lpos.data(), em.merge_lpos.size() * 4);
     put(L.mask_words, em.mask_words.data(), em.mask_words.size() * 4);
+    put(L.score_items, em.score_items.data(), em.score_items.size() * sizeof(fa::Item));
+    put(L.score_units, em.score_units.data(), em.score_units.size() * 4);
+    put(L.occ_pos, em.occ_pos.data(), em.occ_pos.size() * 4);
+    put(L.row_pos, em.row_pos.data(), em.row_pos.size() * 4);
+    put(L.entry_off, em.entry_off.data(), em.entry_off.size() * 4);
+    put(L.word_off, em.word_off.data(), em.word_off.size() * 4);
     plan->partial_rows = prow;
+    plan->representatives = in.reps;
     return FA_OK;
 }
 
@@ -655,13 +724,14 @@ extern "C" int fork_attn_plan_create(const fa_dims *dims, const fa_desc *desc,
     if (!dims || !desc || !out_plan) return FA_ERR_NULL;
     try {
         Input in{dims, desc, 0, {}, {}};
-        int rc = validate(in);
-        if (rc != FA_OK) return rc;
         fa_plan_opts o;
         std::memset(&o, 0, sizeof o);
         if (opts) o = *opts;
+        in.reps = o.representatives == 1;
+        int rc = validate(in);
+        if (rc != FA_OK) return rc;
         if (o.chunk_pages < 0 || o.num_sms < 0 || o.tensor_ctas < 0 || o.tensor_chunk_pages < 0 ||
-            o.reserved[0] || o.reserved[1] || o.reserved[2])
+            (o.representatives != 0 && o.representatives != 1) || o.reserved[0] || o.reserved[1])
             return FA_ERR_INVALID;
         fa_plan *p = new fa_plan();
         p->dims = *dims;
@@ -686,7 +756,7 @@ extern "C" int fork_attn_plan_create(const fa_dims *dims, const fa_desc *desc,
 extern "C" int fork_attn_plan_sizes(const fa_plan *plan, size_t *plan_bytes, size_t *scratch_bytes) {
     if (!plan || !plan_bytes || !scratch_bytes) return FA_ERR_NULL;
     *plan_bytes = size_t(plan->lay.total);
-    *scratch_bytes = size_t(fa::scratch_bytes(plan->partial_rows));
+    *scratch_bytes = size_t(fa::plan_scratch_bytes(plan));
     return FA_OK;
 }
 

@@ -14,6 +14,7 @@ struct fa_plan {
     fa::Layout lay;
     std::vector<uint8_t> blob;    // host copy of the device plan buffer (lay.total bytes)
     int64_t partial_rows;         // fp32 partial rows (each 128 floats + 1 lse)
+    bool representatives;         // a plan of representative queries (key scoring)
     fa_plan_stats stats;
     int32_t tc_ctas;              // persistent CTAs of the tcgen05 kernel (<= SMs)
     // set by fork_attn_plan_upload
@@ -34,5 +35,12 @@ inline int64_t scratch_lse_offset(int64_t partial_rows) {
 inline int64_t scratch_bytes(int64_t partial_rows) {
     if (partial_rows == 0) return 0;
     return scratch_lse_offset(partial_rows) + ((partial_rows * 4 + kAlign - 1) / kAlign) * kAlign;
+}
+// A scoring plan's scratch holds, after the partials, the per-KV-head key scores:
+// Hkv x total_entries fp32.
+inline int64_t score_part_offset(const fa_plan *p) { return scratch_bytes(p->partial_rows); }
+inline int64_t plan_scratch_bytes(const fa_plan *p) {
+    const int64_t sc = p->representatives ? int64_t(p->dims.num_kv_heads) * p->lay.total_entries * 4 : 0;
+    return scratch_bytes(p->partial_rows) + ((sc + kAlign - 1) / kAlign) * kAlign;
 }
 }  // namespace fa

@@ -33,6 +33,7 @@ struct Occ {
     int32_t lpos0;
     int32_t mask_off;
     int32_t prow_base;
+    int32_t pos_off;  // representative plans: its pages' score positions at occ_pos[pos_off ..]
 };
 
 // A work item: one chunk, one KV head, and a row group = rows[row_off .. row_off + n_rows)
@@ -98,13 +99,27 @@ static_assert(sizeof(QMerge) == 64, "one 64-byte record per query token");
 // Byte offsets of the arrays inside the device plan buffer.  The first 256 bytes are a
 // header of int32 words, zero in the uploaded plan: [0] the device error word, [1] [2] the
 // work counter and exit count of the persistent tcgen05 kernel (its last CTA puts both back
-// to zero); the other words are unused and stay zero.
+// to zero), [3] the work counter of the scoring kernel (set to zero before each launch); the
+// other words are unused and stay zero.
+//
+// Plans of representative queries (for key scoring) also hold: every work item once more in
+// one list (score_items), cut into units of at most kScoreUnitTiles 128-key tiles (score_units:
+// item, first tile, tiles, 0), for every reader of every chunk page the score index of the
+// page's slot 0 for that reader (occ_pos: entry_off[branch] + the logical position of slot 0,
+// pages in chunk order, one run per occurrence), each row's occurrence run in it (row_pos),
+// and per branch the offsets of its entries (entry_off) and of its keep-bit words (word_off).
+// A chunk's pages need not be logically adjacent (a run may step over pages its readers do
+// not see), so the positions are listed per page.
 struct Layout {
     int64_t chunk_pages, chunks, items_rows, items_tc, items_r8, rows, branches, q_merge, merge_bases,
-        merge_lpos, mask_words, total;
+        merge_lpos, mask_words, score_items, score_units, occ_pos, row_pos, entry_off, word_off, total;
     int32_t n_chunk_pages, n_chunks, n_items_rows, n_items_tc, n_items_r8, n_rows, n_branches, total_q,
-        n_merge_bases, n_mask_words;
+        n_merge_bases, n_mask_words, n_score_items, n_score_units;
+    int64_t total_entries, total_words;
 };
+
+// Tiles of one unit of the scoring kernel's work queue.
+constexpr int kScoreUnitTiles = 16;
 
 // Device error word bits (header word 0), and which kernel set them.
 enum : int32_t {
@@ -113,6 +128,7 @@ enum : int32_t {
     kErrTc = 4,        // ... in the tcgen05 kernel
     kErrRow8 = 8,      // ... in the row kernel for <= 8 rows
     kErrRow = 16,      // ... in the row kernel for <= 32 rows
+    kErrScore = 32,    // ... in the key-scoring kernel
 };
 
 }  // namespace fa

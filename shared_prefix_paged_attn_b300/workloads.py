@@ -355,6 +355,27 @@ SMALL = {1: dict(shrink=1), 2: dict(shrink=8), 3: dict(shrink=16), 4: dict(shrin
          5: dict(shrink=8, requests=4)}
 
 
+def with_representatives(w: Workload, branches: Optional[List[int]] = None, reps: int = 32,
+                         device: str = "cpu") -> Workload:
+    """The cache of ``w`` restricted to ``branches`` (all by default), each with ``reps``
+    representative queries of its own: N(0, 1) fp32 cast to bf16, drawn after the workload's
+    own values from seed + 7.
+
+    AgentKV blog (rit.work), "Как AgentKV выбирает и освобождает записи кэша": the queries kept
+    per phase are merged into one set of representatives (32 in the main experiments) that
+    scores every key before a compression."""
+    sub = subset(w, list(range(w.num_branches)) if branches is None else list(branches))
+    B = sub.num_branches
+    sub.branch_q_off = (np.arange(B + 1, dtype=np.int64) * reps).astype(np.int32)
+    sub.name = w.name + f"_reps{reps}"
+    sub.meta = dict(sub.meta, reps=reps)
+    gen = torch.Generator(device=device).manual_seed(int(w.meta["seed"]) + 7)
+    sub.q = torch.randn((B * reps, w.num_q_heads, w.head_dim), generator=gen, device=device,
+                        dtype=torch.float32).to(torch.bfloat16)
+    sub.k_pages, sub.v_pages = sub.k_pages.to(device), sub.v_pages.to(device)
+    return sub
+
+
 # Workload 6: the prefill-shaped one (every token a query), beside the five decodes.
 PREFILL = 6
 

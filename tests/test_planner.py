@@ -104,8 +104,10 @@ def test_reserved_planner_fields_must_be_zero():
     handle = ctypes.c_void_p()
     for i in range(4):
         opts = _lib.FaPlanOpts()
-        if i < 3:
+        if i < 2:
             opts.reserved[i] = 1
+        elif i == 2:
+            opts.representatives = 2  # only 0 or 1
         rc = lib.fork_attn_plan_create(ctypes.byref(dims), ctypes.byref(desc), ctypes.byref(opts),
                                        ctypes.byref(handle))
         assert rc == (-2 if i < 3 else 0)
@@ -275,3 +277,26 @@ def test_packed_dag_prefill_plan(chunk_pages):
         assert st["items_skipped"] > 0
     full = fa.plan_for(W.packed_dag_prefill(values=False)).stats()
     assert full["num_items_tensor"] > 0 and full["num_items_rows"] == 0
+
+
+def test_representatives_plans():
+    # representative queries see the whole list: n_q may exceed n_b, every (row, visible
+    # entry) pair counts, a branch's rows (n_q x G) must fit one 256-row group
+    w = W.make(2, small=True)
+    ws = W.with_representatives(w, list(range(3)), reps=32)
+    st = fa.plan_for(ws, representatives=1).stats()
+    G = ws.num_q_heads // ws.num_kv_heads
+    vis = sum(len(__import__("oracle.compact", fromlist=["x"]).kept_indices(ws, b)) for b in range(3))
+    assert st["flops_rows"] + st["flops_tensor"] == vis * 32 * G * ws.num_kv_heads * 4 * 128
+    assert st["num_items_rows"] == 0 and st["num_items_tensor"] > 0
+    E, nw = fa.fork_attn_score_sizes(fa.plan_for(ws, representatives=1))
+    assert E == sum(ws.branch_len(b) for b in range(3))
+    assert nw == sum((ws.branch_len(b) + 31) // 32 for b in range(3))
+    with pytest.raises(fa.ForkAttnError):
+        fa.fork_attn_score_sizes(fa.plan_for(w))  # a decode plan has no scores
+    tiny = W.random_dag(5, n_branches=2, max_seg_len=10, values=True)
+    t = W.with_representatives(tiny, reps=40)  # more representatives than entries
+    assert _plan_rc(t, representatives=1) == 0
+    assert _plan_rc(t) == -2
+    big = W.with_representatives(W.make(4, small=True), [0], reps=33)  # 33 x 8 rows > 256
+    assert _plan_rc(big, representatives=1) == -3
