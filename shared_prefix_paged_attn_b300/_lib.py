@@ -3,7 +3,10 @@ import ctypes
 import os
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(HERE, "libforkattn.so")
+# FORK_ATTN_CHECKED=1 in the environment (read at the first load) selects the build with
+# device bounds checks on every index taken from a plan buffer
+LIB_PATH = os.path.join(HERE, "libforkattn_checked.so" if os.environ.get("FORK_ATTN_CHECKED") == "1"
+                        else "libforkattn.so")
 
 c_int32, c_int64, c_float, c_void_p = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p
 

@@ -6,6 +6,8 @@ import sys
 HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libforkattn.so")
+# the same sources with device bounds checks on every page id and row record from the plan
+LIB_CHECKED = os.path.join(HERE, "libforkattn_checked.so")
 SOURCES = ["plan.cpp", "decode.cu", "compact.cu", "score.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -16,17 +18,20 @@ def _newest_source_mtime() -> float:
     return max(os.path.getmtime(p) for p in paths)
 
 
-def build(force: bool = False, verbose_ptxas: bool = False) -> str:
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= _newest_source_mtime():
-        return LIB
+def build(force: bool = False, verbose_ptxas: bool = False, checked: bool = False) -> str:
+    out = LIB_CHECKED if checked else LIB
+    if not force and os.path.exists(out) and os.path.getmtime(out) >= _newest_source_mtime():
+        return out
     cmd = ["nvcc", *ARCH, "-O3", "-std=c++17", "-lineinfo", "-shared", "-Xcompiler", "-fPIC",
-           "-Xcompiler", "-Wall", "-o", LIB]
+           "-Xcompiler", "-Wall", "-o", out]
+    if checked:
+        cmd.append("-DFORK_ATTN_CHECKED")
     if verbose_ptxas:
         cmd += ["-Xptxas", "-v"]
     cmd += [os.path.join(CSRC, s) for s in SOURCES]
     subprocess.run(cmd, check=True)
-    return LIB
+    return out
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose_ptxas="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose_ptxas="-v" in sys.argv, checked="--checked" in sys.argv))

@@ -86,6 +86,8 @@ int fill_params(const fa_plan *plan, const void *q, const void *k_pages, const v
     p.pool_pages = int32_t(plan->num_pages_pool);
     p.tc_ctas = plan->tc_ctas;
     p.total_rows = L.total_q * plan->dims.num_q_heads;
+    p.n_partial_rows = int32_t(plan->partial_rows);
+    p.n_mask_words = L.n_mask_words;
     return FA_OK;
 }
 

@@ -42,6 +42,12 @@ __global__ void __launch_bounds__(kThreads, 6) merge_kernel(const __grid_constan
     const int n = r0.y, i = r0.w, pos = r1.x;
     const int g = h / p.G, jh = h % p.G;
     const int off = (i * p.G + jh) * p.Hkv + g;
+    // checked build: a partial row outside the scratch is flagged and left out
+    auto row_ok = [&](int pr) {
+        if (!kChecked || (pr >= 0 && pr < p.n_partial_rows)) return true;
+        atomicOr(p.err, kErrBounds | kErrMerge);
+        return false;
+    };
 
     if (n <= kMergeInline) {
         // every partial's lse and its O slice loaded at once, then summed in the plan's order
@@ -51,7 +57,7 @@ __global__ void __launch_bounds__(kThreads, 6) merge_kernel(const __grid_constan
         float4 v[kMergeInline];
 #pragma unroll
         for (int k = 0; k < kMergeInline; ++k) {
-            const bool use = k < n && lpos[k] <= pos;
+            const bool use = k < n && lpos[k] <= pos && row_ok(base[k] + off);
             ls[k] = use ? p.part_lse[base[k] + off] : -INFINITY;
             v[k] = use ? *reinterpret_cast<const float4 *>(p.part_o + size_t(base[k] + off) * kHeadDim + lane * 4)
                        : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -83,7 +89,7 @@ __global__ void __launch_bounds__(kThreads, 6) merge_kernel(const __grid_constan
     const int32_t *lp = p.merge_lpos + r0.x;
     // a partial whose chunk starts after the token holds nothing it sees (and may never have
     // been written): it gets weight zero
-    auto seen = [&](int k) { return __ldg(lp + k) <= pos; };
+    auto seen = [&](int k) { return __ldg(lp + k) <= pos && row_ok(bases[k] + off); };
 
     // partial k's lse sits in lane k % 32 (rounds of 32); max and weights by shuffles
     float M = -INFINITY;

@@ -129,6 +129,7 @@ enum : int32_t {
     kErrRow8 = 8,      // ... in the row kernel for <= 8 rows
     kErrRow = 16,      // ... in the row kernel for <= 32 rows
     kErrScore = 32,    // ... in the key-scoring kernel
+    kErrMerge = 64,    // ... in the merge kernel
 };
 
 }  // namespace fa

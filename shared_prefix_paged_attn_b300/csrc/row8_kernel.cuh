@@ -88,6 +88,7 @@ __global__ void __launch_bounds__(kThreads, 3) row8_kernel(const __grid_constant
         if (tid < it.n_rows) {
             const int4 rec = __ldg(reinterpret_cast<const int4 *>(p.rows + it.row_off + tid));
             ri = RowInfo{rec.x + it.head * p.G, rec.y, rec.z, rec.w < 0 ? -1 : rec.w + it.head};
+            checked_row(p, ri.qrow, ri.prow, ri.mask_off, n_pages, kErrRow8);
             row_needs_mask = ri.mask_off >= 0 || ri.climit < kPageSize * n_pages - 1;
         }
         sm.rows[tid] = ri;
@@ -114,7 +115,7 @@ __global__ void __launch_bounds__(kThreads, 3) row8_kernel(const __grid_constant
     // current batch b, and the next batch is already loaded, so issuing never waits on them
     auto pid_at = [&](int i) -> int32_t {
         const int k = warp + kWarps * i;
-        return k < n_pages ? __ldg(pages + k) : 0;
+        return k < n_pages ? checked_page(p, __ldg(pages + k), kErrRow8) : 0;
     };
     int32_t pid_cur = pid_at(lane), pid_nxt = pid_at(32 + lane);
     int issued = 0;

@@ -84,7 +84,7 @@ __device__ __forceinline__ void run_pages(const DecodeParams &p, Smem &sm, const
     // current batch b, and the next batch is already loaded, so issuing never waits on them
     auto pid_at = [&](int i) -> int32_t {
         const int k = warp + kWarps * i;
-        return k < n_pages ? __ldg(pages + k) : 0;
+        return k < n_pages ? checked_page(p, __ldg(pages + k), kErrRow) : 0;
     };
     int32_t pid_cur = pid_at(lane), pid_nxt = pid_at(32 + lane);
     int issued = 0;
@@ -281,6 +281,7 @@ __global__ void __launch_bounds__(kThreads, 2) row_kernel(const __grid_constant_
             ri.climit = rec.y;
             ri.mask_off = rec.z;
             ri.prow = rec.w < 0 ? -1 : rec.w + it.head;
+            checked_row(p, ri.qrow, ri.prow, ri.mask_off, ch.n_pages, kErrRow);
             row_needs_mask = ri.mask_off >= 0 || ri.climit < kPageSize * ch.n_pages - 1;
         }
         sm.rows[tid] = ri;

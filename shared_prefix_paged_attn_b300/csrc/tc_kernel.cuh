@@ -96,7 +96,9 @@ struct Row {
 // Row r of a work item -> (query row, causal limit in chunk tokens, visibility words, partial row).
 __device__ __forceinline__ Row item_row(const DecodeParams &p, const Item &it, int r) {
     const int4 rec = __ldg(reinterpret_cast<const int4 *>(p.rows + it.row_off + r));
-    return Row{rec.x + it.head * p.G, rec.y, rec.z, rec.w < 0 ? -1 : rec.w + it.head};
+    Row row{rec.x + it.head * p.G, rec.y, rec.z, rec.w < 0 ? -1 : rec.w + it.head};
+    checked_row(p, row.qrow, row.prow, row.mask_off, it.n_pages, kErrTc);
+    return row;
 }
 
 // Producer warp: lanes 0-7 each read one page id of the tile and issue that page's two
@@ -141,6 +143,10 @@ __device__ __forceinline__ void producer(const DecodeParams &p, Smem &sm, const 
     for (int i = 0; i < kMaxChunkPages / 32; ++i) {
         const int idx = 32 * i + lane;
         pid[i] = idx < ch.n_pages ? __ldg(pages + idx) : p.pool_pages;
+        if (kChecked && idx < ch.n_pages && (pid[i] < 0 || pid[i] >= p.pool_pages)) {
+            atomicOr(p.err, kErrBounds | kErrTc);  // read as the zero-filled page past the pool
+            pid[i] = p.pool_pages;
+        }
     }
     // page of tile j seen by lane l < 8: index 8 j + l, held by lane 8 (j % 4) + l in pid[j / 4]
     auto page_of = [&](int j) -> int32_t {

@@ -54,3 +54,13 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(_lib, "_LIB", None)
     with pytest.raises(ImportError):
         _lib.load()
+
+
+def test_checked_build_exports_the_same_symbols():
+    # the library with device bounds checks is the same C ABI
+    import ctypes
+    from shared_prefix_paged_attn_b300 import _lib, build
+    path = build.build(checked=True)
+    lib = ctypes.CDLL(path)
+    for name in _lib.SIGNATURES:
+        assert hasattr(lib, name), name
