@@ -211,9 +211,9 @@ int fork_attn_decode(const void *q, const void *k_pages, const void *v_pages,
  * fork_attn_decode itself runs the kernels overlapped, all on `stream`: the tcgen05 kernel
  * first, then the row kernels as programmatic dependent launches (they start once every
  * tcgen05 CTA has started, and take the SMs it leaves and frees), then the merge as an
- * ordinary launch after all of them.  No helper stream or event is involved, so a decode can
- * be captured into a CUDA graph; an event recorded between those kernels would only order
- * them, which is why this call runs them one by one instead. */
+ * ordinary launch after all of them, with no helper stream or event; an event recorded
+ * between those kernels would order them (and so serialise them), which is why this call
+ * runs them one by one instead. */
 int fork_attn_decode_timed(const void *q, const void *k_pages, const void *v_pages,
                            const fa_plan *plan, void *out, float *lse, void *stream,
                            void **events, int32_t n_events);
@@ -248,8 +248,7 @@ int fork_attn_check(fa_plan *plan, int32_t *device_error, void *stream);
  * no cudaFree, no allocating library routine.
  *
  * The first call on a device (made current by the caller) looks up the array's device
- * address with cudaGetSymbolAddress; make that first call before any stream capture.
- * Every call on a device shares the one array and leaves the last call's contents in it:
+ * address with cudaGetSymbolAddress.  Every call on a device shares the one array and leaves the last call's contents in it:
  * two calls whose work overlaps on the GPU (different streams, or different host threads)
  * race on it, so serialise them.  fork_attn_check on the same plan reads and clears the
  * device error word this call wrote (word 0 of the array), until another call overwrites it.
