@@ -207,14 +207,19 @@ def dist_setup(n_gpus):
 
 def rank_workload(config, rank, device, values=True, split="none", world=1):
     """Rank r's problem.  split "none": the workload's structure with values drawn from
-    seed + 1000 r (independent problems, one per GPU: weak scaling).  split "head" or
-    "request": rank r's share of the one workload, by KV head or by request (strong
-    scaling).  Neither has a collective on the data path."""
+    seed + 1000 r (independent problems, one per GPU: weak scaling).  split "head",
+    "request" or "sequence": rank r's share of the one workload (strong scaling); only the
+    split by sequence exchanges data (an all-gather of partials in each step)."""
     if split != "none" and world > 1:
         from shared_prefix_paged_attn_b300 import shard
         w = W.make(config, device=device, values=values)
         cid = config
-        w = shard.split_by_kv_head(w, rank, world) if split == "head" else shard.split_by_request(w, rank, world)[0]
+        if split == "head":
+            w = shard.split_by_kv_head(w, rank, world)
+        elif split == "request":
+            w = shard.split_by_request(w, rank, world)[0]
+        else:
+            w = shard.split_by_sequence(w, rank, world)
         w.meta["config_id"] = cid
         return w
     w = W.make(config, device=device, values=values and rank == 0)
@@ -265,11 +270,17 @@ def host_copy(w):
     return (w.q.cpu().pin_memory(), w.k_pages.cpu().pin_memory(), w.v_pages.cpu().pin_memory())
 
 
-def workload_config(w, unique_bytes):
-    """The `config` dict of a bench line: the same keys and values in both arms."""
+def workload_config(w, unique_bytes, touched_pages):
+    """The `config` dict of a bench line: the same keys and values in both arms.  Besides the
+    unique-KV bytes (the metric's numerator), the touched-page bytes (whole pages holding a
+    visible slot) and the per-step bytes of Q, out (bf16), LSE and the plan's records are
+    reported apart."""
+    hd = w.head_dim
     return {"workload": w.name, "config_id": int(w.meta.get("config_id", 0)),
             "Hq": w.num_q_heads, "Hkv": w.num_kv_heads, "branches": w.num_branches,
             "total_q": w.total_q, "unique_kv_bytes": int(unique_bytes),
+            "touched_page_bytes": int(touched_pages) * w.num_kv_heads * w.page_size * hd * 2 * 2,
+            "qol_bytes": int(w.total_q * w.num_q_heads * (hd * 2 + hd * 2 + 4)),
             "l2": "flushed (256 MiB write) between steps"}
 
 
@@ -283,7 +294,8 @@ def run_reference(args):
     w = W.make(args.config, device=dev)
     w.meta["config_id"] = args.config
     w.q, w.k_pages, w.v_pages = w.q.cpu(), w.k_pages.cpu(), w.v_pages.cpu()
-    unique_bytes = oracle.unique_slots(w)[0] * w.num_kv_heads * KV_BYTES_PER_SLOT_HEAD
+    uslots, upages = oracle.unique_slots(w)
+    unique_bytes = uslots * w.num_kv_heads * KV_BYTES_PER_SLOT_HEAD
     Hq, Hkv = w.num_q_heads, w.num_kv_heads
     G = Hq // Hkv
     times = []
@@ -302,7 +314,7 @@ def run_reference(args):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": workload_config(w, unique_bytes),
+            "config": workload_config(w, unique_bytes, upages),
             "cpu_baseline": {"value": value, "unit": "GB/s", "cores": oracle.threads_default(),
                              "kind": "oracle",
                              "sample": "per step one (branch, KV head) of the workload, fp64 "
@@ -352,17 +364,32 @@ def measure_config(cfg, args, dev, flush, dist, rank, world, steps, keep=False):
     split = getattr(args, "split", "none")
     w = rank_workload(cfg, rank, str(dev), split=split, world=world)
     w.meta["config_id"] = cfg
+    seq = split == "sequence"
     t0 = time.perf_counter()
-    run = fa.ForkAttention(w, out_dtype=fa.FA_BF16, device=dev)
+    # a split by sequence decodes fp32 partials of every row, gathered and merged each step
+    run = fa.ForkAttention(w, out_dtype=fa.FA_F32 if seq else fa.FA_BF16, device=dev)
     plan_s = time.perf_counter() - t0
     st = run.plan.stats()
     unique_bytes = st["unique_visible_slots"] * w.num_kv_heads * KV_BYTES_PER_SLOT_HEAD
     stream = torch.cuda.current_stream(dev)
     q, k, v = w.q, w.k_pages, w.v_pages
+    if seq:
+        g_out = torch.empty((world,) + tuple(run.out.shape), dtype=torch.float32, device=dev)
+        g_lse = torch.empty((world,) + tuple(run.lse.shape), dtype=torch.float32, device=dev)
+        final_out = torch.empty(tuple(run.out.shape), dtype=torch.bfloat16, device=dev)
+        final_lse = torch.empty(tuple(run.lse.shape), dtype=torch.float32, device=dev)
 
     def step(events=None):
         if events is None:
             fa.fork_attn_decode(q, k, v, run.plan, run.out, run.lse, stream)
+            if seq:  # the split's one exchange: every rank's partials, then the merge
+                if dist:
+                    dist.all_gather_into_tensor(g_out, run.out)
+                    dist.all_gather_into_tensor(g_lse, run.lse)
+                else:
+                    g_out[0].copy_(run.out)
+                    g_lse[0].copy_(run.lse)
+                fa.fork_attn_merge_parts(g_out, g_lse, final_out, final_lse, stream)
         else:
             fa.fork_attn_decode_timed(q, k, v, run.plan, run.out, run.lse, events, stream)
 
@@ -410,17 +437,22 @@ def measure_config(cfg, args, dev, flush, dist, rank, world, steps, keep=False):
            for j in range(len(KERNEL_NAMES))]
     kernels = kernel_rooflines(st, w, avg, ncu_traffic(w.name))
     hbm_peak, _ = peaks()
-    # whole-job unique KV bytes: every rank's own problem (weak), or the shares of one
-    # problem, which add up to it (strong)
-    job_bytes = unique_bytes * world if split == "none" else sum_over_ranks(dist, unique_bytes, dev)
-    job_q = w.total_q * world if split == "none" else sum_over_ranks(dist, w.total_q, dev)
+    # whole-job unique KV bytes: every rank's own problem (weak), or the one problem the ranks
+    # share (strong: its own count, as a split by sequence may read a mounted page twice)
+    if split == "none":
+        job_bytes, job_q = unique_bytes * world, w.total_q * world
+    else:
+        wf = W.make(cfg, values=False)
+        job_bytes = fa.plan_for(wf).stats()["unique_visible_slots"] * wf.num_kv_heads * KV_BYTES_PER_SLOT_HEAD
+        job_q = wf.total_q
     value = job_bytes / (ms_max * 1e-3) / 1e9
     res = {"cfg": cfg, "w": w if keep else None, "run": run if keep else None, "stats": st,
            "unique_bytes": unique_bytes, "plan_s": plan_s, "ms": ms_max, "step_ms": step_ms,
            "wall": wall, "value": value, "bq_s": job_q / (ms_max * 1e-3),
            "frac": value / world / hbm_peak, "kernels": kernels,
            "kernel_ms": {n: a for n, a, p in zip(KERNEL_NAMES, avg, kernels_present(st)) if p},
-           "clocks": clk.record(), "config": workload_config(w, unique_bytes), "Kk": Kk,
+           "clocks": clk.record(), "config": workload_config(w, unique_bytes, st["touched_pages"]),
+           "plan_bytes": run.plan.sizes()[0], "scratch_bytes": run.plan.sizes()[1], "Kk": Kk,
            "launches_per_step": sum(kernels_present(st))}
     if not keep:
         del run, w, q, k, v
@@ -606,6 +638,7 @@ def run_ours(args):
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": head["config"],
             "plan_s": head["plan_s"],
+            "plan_bytes": head["plan_bytes"], "scratch_bytes": head["scratch_bytes"],
             "branch_queries_per_s": head["bq_s"],
             "frac_of_hbm_peak": head["frac"],
             "roofline": roof,
@@ -705,9 +738,10 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-per-config", action="store_true",
                     help="time only --config (the line's per_config then stays empty)")
-    ap.add_argument("--split", choices=["none", "head", "request"], default="none",
+    ap.add_argument("--split", choices=["none", "head", "request", "sequence"], default="none",
                     help="with N > 1: every rank its own problem (none, weak scaling) or a share "
-                         "of one problem by KV head or by request (strong scaling)")
+                         "of one problem by KV head, by request or by sequence (strong scaling; "
+                         "the sequence split all-gathers partials and merges them every step)")
     ap.add_argument("--no-scoring", action="store_true",
                     help="leave out the key-scoring entry of the line")
     ap.add_argument("--no-prefill", action="store_true",

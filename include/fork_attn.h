@@ -332,6 +332,21 @@ int fork_attn_compact_run(const fa_compact *c, void *k_pages, void *v_pages, voi
 /* Frees the compaction plan (not the caller's device buffers). */
 int fork_attn_compact_destroy(fa_compact *c);
 
+/* Joins the results of one problem split into parts that each saw a disjoint share of every
+ * branch's visible entries (for instance one range of logical positions per GPU, each part
+ * decoded with the other entries' visibility bits cleared): part_out [device, fp32,
+ * n_parts x rows x head_dim (128)] and part_lse [device, fp32, n_parts x rows], part k's rows
+ * at k * rows; rows = total_q x Hq.  Per row, the log-sum-exp merge of the parts in order
+ * (Agentrix (gitlink.org.cn), "初赛基础与决赛演进": per-branch results are merged):
+ *     L = max_k lse_k + ln sum_k exp(lse_k - max_k lse_k),   out = sum_k exp(lse_k - L) out_k,
+ * a part with lse = -inf contributing nothing; a row no part saw gets out = 0, lse = -inf.
+ * out [device, rows x 128, bf16 (RNE) or fp32 by out_dtype], lse [device, fp32, rows], on
+ * `stream`; no allocation, no synchronisation.  Errors: FA_ERR_NULL, FA_ERR_INVALID (n_parts
+ * < 1, rows < 0, bad out_dtype), FA_ERR_ALIGN (part_out, out not 16-byte aligned),
+ * FA_ERR_CUDA. */
+int fork_attn_merge_parts(const float *part_out, const float *part_lse, int32_t n_parts,
+                          int64_t rows, void *out, int32_t out_dtype, float *lse, void *stream);
+
 /* ---- Key scoring by representative queries, and top-k keep ----
  * AgentKV blog (rit.work), "Как AgentKV выбирает и освобождает записи кэша": the recent
  * queries of every phase are merged into one set of representatives (32 in the main

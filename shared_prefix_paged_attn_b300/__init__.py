@@ -14,7 +14,7 @@ from . import _lib
 from ._lib import FA_BF16, FA_F32, FaCompactDims, FaDesc, FaDims, FaPlanOpts, FaPlanStats
 
 __all__ = ["ForkAttnError", "Plan", "fork_attn_plan_create", "fork_attn_decode",
-           "fork_attn_decode_timed", "fork_attn_decode_static_scratch", "fork_attn_score",
+           "fork_attn_decode_timed", "fork_attn_decode_static_scratch", "fork_attn_merge_parts", "fork_attn_score",
            "fork_attn_topk", "fork_attn_score_sizes", "KeyScorer", "fork_attn_check",
            "fork_attn_strerror", "FA_BF16", "FA_F32", "plan_for", "ForkAttention", "CompactPlan", "fork_attn_compact_create", "fork_attn_compact_upload", "fork_attn_compact_run"]
 
@@ -161,6 +161,17 @@ def fork_attn_decode_static_scratch(q, k_pages, v_pages, plan: Plan, out, lse, s
                                                        plan.handle, _ptr(out), _ptr(lse),
                                                        _stream_ptr(stream)),
            "fork_attn_decode_static_scratch")
+
+
+def fork_attn_merge_parts(part_out, part_lse, out, lse, stream=None):
+    """fork_attn_merge_parts: part_out [n_parts, rows, 128] fp32 and part_lse [n_parts, rows]
+    (device tensors, or [n_parts, total_q, Hq, ...]) into out (bf16 or fp32) and lse."""
+    import torch
+    n_parts = int(part_lse.shape[0])
+    rows = int(part_lse.numel() // n_parts)
+    odt = FA_F32 if out.dtype == torch.float32 else FA_BF16
+    _check(_lib.load().fork_attn_merge_parts(_ptr(part_out), _ptr(part_lse), n_parts, rows, _ptr(out), odt,
+                                             _ptr(lse), _stream_ptr(stream)), "fork_attn_merge_parts")
 
 
 def fork_attn_score(q, k_pages, plan: Plan, lse, scores, stream=None):

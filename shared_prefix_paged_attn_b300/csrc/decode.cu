@@ -290,3 +290,16 @@ extern "C" int fork_attn_decode_static_scratch(const void *q, const void *k_page
     plan->err_word = p.err;  // fork_attn_check reads this call's error word
     return launch_all(p, plan, st, nullptr, true);  // nothing is created here
 }
+
+extern "C" int fork_attn_merge_parts(const float *part_out, const float *part_lse, int32_t n_parts, int64_t rows,
+                                     void *out, int32_t out_dtype, float *lse, void *stream) {
+    if (!part_out || !part_lse || !out || !lse) return FA_ERR_NULL;
+    if (n_parts < 1 || rows < 0 || (out_dtype != FA_BF16 && out_dtype != FA_F32)) return FA_ERR_INVALID;
+    if (!aligned(part_out, 16) || !aligned(out, 16) || !aligned(part_lse, 4) || !aligned(lse, 4)) return FA_ERR_ALIGN;
+    if (rows == 0) return FA_OK;
+    const int64_t blocks = (rows * 32 + fa::mergek::kThreads - 1) / fa::mergek::kThreads;
+    if (blocks > INT32_MAX) return FA_ERR_INVALID;
+    fa::mergek::merge_parts_kernel<<<unsigned(blocks), fa::mergek::kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+        part_out, part_lse, n_parts, rows, out, out_dtype, lse);
+    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}

@@ -143,3 +143,47 @@ __global__ void __launch_bounds__(kThreads, 6) merge_kernel(const __grid_constan
 
 }  // namespace mergek
 }  // namespace fa
+
+namespace fa {
+namespace mergek {
+
+// Merge of whole per-part results of the same query rows (a problem split into parts that
+// each saw a disjoint share of every branch's entries, for instance one range of logical
+// positions per GPU): part k holds out_k [rows][128] fp32 and lse_k [rows]; the same log-sum-
+// exp merge as above, parts in order, one warp per row.
+__global__ void __launch_bounds__(kThreads) merge_parts_kernel(const float *part_out, const float *part_lse,
+                                                               int32_t n_parts, int64_t rows, void *out,
+                                                               int32_t out_dtype, float *lse) {
+    const int64_t row = (int64_t(blockIdx.x) * kThreads + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (row >= rows) return;
+    float M = -INFINITY;
+    for (int k0 = 0; k0 < n_parts; k0 += 32)
+        if (k0 + lane < n_parts) M = fmaxf(M, part_lse[size_t(k0 + lane) * rows + row]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float L = 0.f;
+    if (M != -INFINITY) {
+        for (int k = 0; k < n_parts; ++k) {
+            const float l = part_lse[size_t(k) * rows + row];
+            if (l == -INFINITY) continue;  // the part saw nothing of this row
+            const float w = expf(l - M);
+            const float4 v = *reinterpret_cast<const float4 *>(part_out + (size_t(k) * rows + row) * kHeadDim + lane * 4);
+            L += w;
+            acc.x += w * v.x; acc.y += w * v.y; acc.z += w * v.z; acc.w += w * v.w;
+        }
+        const float inv = 1.f / L;
+        acc.x *= inv; acc.y *= inv; acc.z *= inv; acc.w *= inv;
+    }
+    if (out_dtype == FA_F32) {
+        *reinterpret_cast<float4 *>(reinterpret_cast<float *>(out) + size_t(row) * kHeadDim + lane * 4) = acc;
+    } else {
+        uint2 pk = make_uint2(ptx::pack_bf16(acc.x, acc.y), ptx::pack_bf16(acc.z, acc.w));
+        *reinterpret_cast<uint2 *>(reinterpret_cast<__nv_bfloat16 *>(out) + size_t(row) * kHeadDim + lane * 4) = pk;
+    }
+    if (lane == 0) lse[row] = (M == -INFINITY) ? -INFINITY : M + logf(L);
+}
+
+}  // namespace mergek
+}  // namespace fa

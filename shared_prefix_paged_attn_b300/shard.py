@@ -2,13 +2,19 @@
 
 Every output row of the decode depends on one query head of one query token and the K/V of
 its KV head over its branch's visible entries, so the problem splits without any exchange on
-the data path, two ways:
+the data path two ways, and a third way with one all-gather:
 
 * by KV head: rank r takes KV heads [r Hkv / N, (r + 1) Hkv / N) and the query heads of their
   groups; every rank reads every page, but only its heads' slices of it.
 * by request: branches that share a physical page (a prefix, a mount) stay on one rank;
   these groups are dealt to the ranks by listed tokens, largest first, each to the rank with
   the fewest so far.  Shared pages are then read by one rank only.
+* by sequence: rank r takes the logical positions [r L / N, (r + 1) L / N) of every branch
+  (L the longest branch), i.e. the same problem with every other entry's visibility bit
+  cleared; positions, and so causal limits, are unchanged, and a shared prefix (the same
+  positions in every branch) falls to one rank per range.  Each rank's result is a partial
+  (out, lse) of every query row; the ranks all-gather them and merge them with the
+  log-sum-exp merge (``fork_attn_merge_parts``): the one split with an exchange.
 
 The outputs concatenate back: by head along the head axis, by request along the query-token
 axis in the ranks' branch order (``gather_rows`` puts them back in the problem's order).
@@ -131,3 +137,35 @@ def gather_rows(parts: List[torch.Tensor], branches: List[List[int]], w: W.Workl
     if not seen.all():
         raise ValueError("the parts do not cover every query token")
     return out
+
+
+def sequence_cuts(w: W.Workload, world: int) -> List[int]:
+    """Logical-position cuts [c_0 = 0, ..., c_N = L] of the split by sequence."""
+    if world < 1:
+        raise ValueError("world must be >= 1")
+    L = max(w.branch_len(b) for b in range(w.num_branches))
+    return [r * L // world for r in range(world + 1)]
+
+
+def split_by_sequence(w: W.Workload, rank: int, world: int) -> W.Workload:
+    """Rank `rank`'s share of `w` by sequence: the same descriptors and values with the
+    visibility bits of every entry outside [c_r, c_{r+1}) cleared."""
+    if not 0 <= rank < world:
+        raise ValueError("rank out of range")
+    lo, hi = sequence_cuts(w, world)[rank:rank + 2]
+    per_branch = []
+    for b in range(w.num_branches):
+        n = w.branch_len(b)
+        j = np.arange(n)
+        if w.vis_bits is None:
+            vis = np.ones(n, dtype=bool)
+        else:
+            words = w.vis_bits[w.vis_word_off[b]:w.vis_word_off[b + 1]].astype(np.uint64)
+            vis = ((words[j // 32] >> (j % 32).astype(np.uint64)) & 1).astype(bool)
+        per_branch.append(vis & (j >= lo) & (j < hi))
+    bits, off = W._pack_branch_bits(per_branch)
+    sub = W.Workload(f"{w.name}_seq{rank}of{world}", w.num_q_heads, w.num_kv_heads, w.page_ids, w.segs,
+                     w.branch_seg_off, w.branch_segs, w.branch_q_off, bits, off, w.num_pages_pool,
+                     meta=dict(w.meta, positions=(lo, hi)))
+    sub.q, sub.k_pages, sub.v_pages = w.q, w.k_pages, w.v_pages
+    return sub

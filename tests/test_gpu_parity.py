@@ -214,3 +214,28 @@ def test_timed_decode_matches_decode_bitwise():
         assert all(t > 0 for t in ms), ms
         out2, lse2 = run(q, k, v)  # and the overlapped decode again after it
         assert torch.equal(out2, base_out) and torch.equal(lse2, base_lse)
+
+
+@pytest.mark.parametrize("cfg", [4, 5])
+@pytest.mark.parametrize("world", [2, 3])
+def test_sequence_split_merged_on_the_device(cfg, world):
+    # the problem split by logical position into `world` parts (each decoded on this GPU
+    # with the other entries hidden), then joined by fork_attn_merge_parts
+    from shared_prefix_paged_attn_b300 import shard
+    w = W.make(cfg, small=True)
+    dev = torch.device("cuda")
+    outs, lses = [], []
+    for r in range(world):
+        sub = shard.split_by_sequence(w, r, world)
+        run = fa.ForkAttention(sub, out_dtype=fa.FA_F32)
+        o, l = run(sub.q.to(dev), sub.k_pages.to(dev), sub.v_pages.to(dev))
+        outs.append(o.clone())
+        lses.append(l.clone())
+    torch.cuda.synchronize()
+    out = torch.empty((w.total_q, w.num_q_heads, w.head_dim), dtype=torch.float32, device=dev)
+    lse = torch.empty((w.total_q, w.num_q_heads), dtype=torch.float32, device=dev)
+    fa.fork_attn_merge_parts(torch.stack(outs), torch.stack(lses), out, lse)
+    torch.cuda.synchronize()
+    ref_out, ref_lse = oracle.fork_attn(w)
+    assert_parity(out.cpu().numpy().reshape(-1, 128), lse.cpu().numpy().reshape(-1), ref_out, ref_lse,
+                  f"config {cfg} in {world} parts")

@@ -146,3 +146,71 @@ def test_request_groups_follow_shared_pages():
     assert shard.head_range(8, 0, 3) == (0, 3) and shard.head_range(8, 2, 3) == (6, 8)
     with pytest.raises(ValueError):
         shard.head_range(2, 0, 4)
+
+
+def _lse_merge(outs, lses):
+    """Log-sum-exp merge of per-part (out, lse) in fp64 (test-side check of the split)."""
+    lses = np.stack(lses)
+    outs = np.stack(outs)
+    M = lses.max(axis=0)
+    fin = np.isfinite(M)
+    w = np.where(np.isfinite(lses), np.exp(lses - np.where(fin, M, 0.0)), 0.0)
+    L = w.sum(axis=0)
+    out = np.where(fin[:, None], (w[..., None] * outs).sum(axis=0) / np.where(fin, L, 1.0)[:, None], 0.0)
+    lse = np.where(fin, M + np.log(np.where(fin, L, 1.0)), -np.inf)
+    return out, lse
+
+
+def _seq_main(rank, world, port, out_dir):
+    # one long shared prefix split by logical position: each rank the oracle's partial of its
+    # range, then the all-gather the split needs (gloo) and the merge
+    os.environ.update(WORLD_SIZE=str(world), RANK=str(rank), LOCAL_RANK=str(rank),
+                      MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    sys.path.insert(0, ROOT)
+    import torch.distributed as dist
+    import oracle
+    from shared_prefix_paged_attn_b300 import shard
+    from shared_prefix_paged_attn_b300 import workloads as W
+    dist.init_process_group("gloo")
+    w = W.make(4, small=True)
+    sub = shard.split_by_sequence(w, rank, world)
+    o, l = oracle.fork_attn(sub, threads=max(1, oracle.threads_default() // world))
+    ot, lt = torch.from_numpy(o), torch.from_numpy(l)
+    go = [torch.empty_like(ot) for _ in range(world)]
+    gl = [torch.empty_like(lt) for _ in range(world)]
+    dist.all_gather(go, ot)
+    dist.all_gather(gl, lt)
+    if rank == 0:
+        np.savez(os.path.join(out_dir, "seq.npz"), o=np.stack([x.numpy() for x in go]),
+                 l=np.stack([x.numpy() for x in gl]))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_split_by_sequence_merges_to_the_whole_problem():
+    import tempfile
+    import oracle
+    from shared_prefix_paged_attn_b300 import workloads as W
+    with tempfile.TemporaryDirectory() as out:
+        mp.start_processes(_seq_main, args=(2, _free_port(), out), nprocs=2, join=True, start_method="spawn")
+        d = np.load(os.path.join(out, "seq.npz"))
+    w = W.make(4, small=True)
+    ref_o, ref_l = oracle.fork_attn(w)
+    o, l = _lse_merge(list(d["o"]), list(d["l"]))
+    assert np.array_equal(np.isneginf(l), np.isneginf(ref_l))
+    fin = ~np.isneginf(ref_l)
+    assert np.abs(o[fin] - ref_o[fin]).max() < 1e-12 and np.abs(l[fin] - ref_l[fin]).max() < 1e-12
+
+
+def test_sequence_split_is_a_partition_of_every_branch():
+    from oracle import compact as C
+    from shared_prefix_paged_attn_b300 import shard
+    from shared_prefix_paged_attn_b300 import workloads as W
+    w = W.make(3, small=True, values=False)
+    for world in (1, 2, 3):
+        parts = [shard.split_by_sequence(w, r, world) for r in range(world)]
+        for b in range(w.num_branches):
+            seen = np.concatenate([C.kept_indices(p, b) for p in parts])
+            assert np.array_equal(np.sort(seen), C.kept_indices(w, b)) and len(set(seen.tolist())) == len(seen)
+    cuts = shard.sequence_cuts(w, 4)
+    assert cuts[0] == 0 and cuts[-1] == max(w.branch_len(b) for b in range(w.num_branches))
