@@ -10,8 +10,9 @@
 // Scores are >= 0, so their fp32 bit patterns order as the values do.  The k-th largest
 // pattern T is found by radix selection over the top 12, middle 12 and low 8 bits (a
 // histogram in shared memory per round, its bins scanned from the top), which also gives how
-// many entries equal to T are kept; a last pass in index order keeps every entry above T and
-// the first of those equal to it (a block-wide prefix count), one 32-bit word per warp.
+// many entries equal to T are kept; a last pass keeps every entry above T and, when not all
+// entries equal to T fit, the first of them in index order (a block-wide prefix count), one
+// 32-bit word per warp.
 #pragma once
 #include <stdint.h>
 
@@ -54,7 +55,7 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const float *scores, con
                                                         uint32_t *keep_bits) {
     __shared__ uint32_t hist[kBins];
     __shared__ uint32_t warp_sums[33];
-    __shared__ uint32_t sel[2];  // selected bin, entries above it
+    __shared__ uint32_t sel[3];  // selected bin, entries above it, entries in it
     const int b = blockIdx.x, tid = threadIdx.x;
     const int64_t e0 = entry_off[b];
     const int n = int(entry_off[b + 1] - e0);
@@ -65,18 +66,32 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const float *scores, con
     uint32_t prefix = 0, mask = 0;
     int64_t remaining = k;
     bool keep_all = false, keep_none = k <= 0;
+    uint32_t n_equal = 0;
     const int shifts[3] = {20, 8, 0};
     const uint32_t widths[3] = {0xFFFu, 0xFFFu, 0xFFu};
     for (int round = 0; round < 3 && !keep_all && !keep_none; ++round) {
         for (int i = tid; i < kBins; i += kThreads) hist[i] = 0;
         __syncthreads();
         const int sh = shifts[round];
-        for (int e = tid; e < n; e += kThreads) {
-            const float s = sc[e];
-            if (s != s) continue;  // not visible
+        const uint32_t wd = widths[round];
+        auto count = [&](float s) {
+            if (s != s) return;  // not visible
             const uint32_t bits = __float_as_uint(s);
-            if ((bits & mask) == prefix) atomicAdd(&hist[(bits >> sh) & widths[round]], 1u);
+            if ((bits & mask) == prefix) atomicAdd(&hist[(bits >> sh) & wd], 1u);
+        };
+        // the entries up to the first 16-byte boundary one by one, then four per load
+        const int head = min(n, int((4 - ((reinterpret_cast<uintptr_t>(sc) >> 2) & 3)) & 3));
+        if (tid < head) count(sc[tid]);
+        const float4 *sc4 = reinterpret_cast<const float4 *>(sc + head);
+        const int n4 = (n - head) >> 2;
+        for (int e = tid; e < n4; e += kThreads) {
+            const float4 v = sc4[e];
+            count(v.x);
+            count(v.y);
+            count(v.z);
+            count(v.w);
         }
+        for (int e = head + 4 * n4 + tid; e < n; e += kThreads) count(sc[e]);
         __syncthreads();
         // bins from the top: thread i sums bins 4095 - 4i .. 4092 - 4i
         uint32_t local = 0;
@@ -95,6 +110,7 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const float *scores, con
                     if (remaining <= int64_t(acc) + hist[bin]) {
                         sel[0] = uint32_t(bin);
                         sel[1] = acc;
+                        sel[2] = hist[bin];
                         break;
                     }
                     acc += hist[bin];
@@ -104,6 +120,7 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const float *scores, con
             prefix |= sel[0] << sh;
             mask |= widths[round] << sh;
             remaining -= sel[1];
+            n_equal = sel[2];  // after the last round: the visible entries equal to T
         }
         __syncthreads();
     }
@@ -112,6 +129,20 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const float *scores, con
     uint32_t carry = 0;
     const int lane = tid & 31, warp = tid >> 5;
     const int n_words = (n + 31) / 32;
+    if (keep_all || keep_none || int64_t(n_equal) <= remaining) {
+        // every entry equal to T is kept too: no order needed, one word per warp at a time
+        for (int wi = warp; wi < n_words; wi += kThreads / 32) {
+            const int e = 32 * wi + lane;
+            bool keep = false;
+            if (e < n && !keep_none) {
+                const float s = sc[e];
+                keep = s == s && (keep_all || __float_as_uint(s) >= T);
+            }
+            const uint32_t word = __ballot_sync(0xffffffffu, keep);
+            if (lane == 0) keep_bits[word_off[b] + wi] = word;
+        }
+        return;
+    }
     for (int base = 0; base < n; base += kThreads) {
         const int e = base + tid;
         bool vis = false, gt = false, eq = false;
