@@ -357,8 +357,9 @@ int fork_attn_merge_parts(const float *part_out, const float *part_lse, int32_t 
  *     score(j) = 1 / (R Hq) * sum over r < R, h < Hq of exp(s_{r,h,j} - lse_{r,h}),
  * s_{r,h,j} = scale <q_{r,h}, K[slot(j), h / G]>, lse_{r,h} over the branch's visible entries
  * (no causal limit).  Three calls on one stream:
- *   1. fork_attn_decode(q, k, v, plan, out, lse, stream): the lse of every representative row
- *      (out is computed too and may be ignored);
+ *   1. fork_attn_score_lse(q, k, plan, lse, stream): the lse of every representative row
+ *      [device, fp32, total_q x Hq] (the decode's kernels with no V, no P V and no output
+ *      rows; fork_attn_decode on the same plan gives the same lse and the outputs too);
  *   2. fork_attn_score(q, k, plan, lse, scores, stream): scores [device, fp32,
  *      total_entries]: branch b's entries at entry_off[b] + j, entry_off the running sum of
  *      the branches' list lengths n_b; an entry the branch does not see is NaN.  Uses the
@@ -368,10 +369,13 @@ int fork_attn_merge_parts(const float *part_out, const float *part_lse, int32_t 
  *      bit j % 32 of word word_off[b] + j / 32 (word_off the running sum of ceil(n_b / 32)),
  *      set for the k_b visible entries with the largest scores, equal scores keeping the
  *      smaller j (all visible entries when k_b >= their number, none when k_b <= 0).
- * q, k_pages, lse: as fork_attn_decode's (16-byte aligned), the same plan, uploaded.  Errors:
+ * q, k_pages, lse: as fork_attn_decode's (16-byte aligned), the same plan, uploaded; the
+ * lse pass writes the plan's scratch partials and its error word.  Errors:
  * FA_ERR_NULL, FA_ERR_INVALID (not a representatives plan), FA_ERR_NOT_UPLOADED,
  * FA_ERR_ALIGN, FA_ERR_CUDA.  fork_attn_plan_create refuses a representatives plan with
  * n_q x G > 256 for a branch (FA_ERR_UNSUPPORTED). */
+int fork_attn_score_lse(const void *q, const void *k_pages, const fa_plan *plan, float *lse,
+                        void *stream);
 int fork_attn_score(const void *q, const void *k_pages, const fa_plan *plan, const float *lse,
                     float *scores, void *stream);
 int fork_attn_topk(const fa_plan *plan, const float *scores, const int32_t *keep_k,

@@ -14,7 +14,7 @@ from . import _lib
 from ._lib import FA_BF16, FA_F32, FaCompactDims, FaDesc, FaDims, FaPlanOpts, FaPlanStats
 
 __all__ = ["ForkAttnError", "Plan", "fork_attn_plan_create", "fork_attn_decode",
-           "fork_attn_decode_timed", "fork_attn_decode_static_scratch", "fork_attn_merge_parts", "fork_attn_score",
+           "fork_attn_decode_timed", "fork_attn_decode_static_scratch", "fork_attn_merge_parts", "fork_attn_score_lse", "fork_attn_score",
            "fork_attn_topk", "fork_attn_score_sizes", "KeyScorer", "fork_attn_check",
            "fork_attn_strerror", "FA_BF16", "FA_F32", "plan_for", "ForkAttention", "CompactPlan", "fork_attn_compact_create", "fork_attn_compact_upload", "fork_attn_compact_run"]
 
@@ -174,6 +174,12 @@ def fork_attn_merge_parts(part_out, part_lse, out, lse, stream=None):
                                              _ptr(lse), _stream_ptr(stream)), "fork_attn_merge_parts")
 
 
+def fork_attn_score_lse(q, k_pages, plan: Plan, lse, stream=None):
+    """fork_attn_score_lse: the representatives' lse [device fp32, total_q x Hq]."""
+    _check(_lib.load().fork_attn_score_lse(_ptr(q), _ptr(k_pages), plan.handle, _ptr(lse), _stream_ptr(stream)),
+           "fork_attn_score_lse")
+
+
 def fork_attn_score(q, k_pages, plan: Plan, lse, scores, stream=None):
     """fork_attn_score: scores [device fp32, total_entries] of every branch's entries."""
     _check(_lib.load().fork_attn_score(_ptr(q), _ptr(k_pages), plan.handle, _ptr(lse), _ptr(scores),
@@ -211,8 +217,8 @@ class KeyScorer:
         self.scores = torch.empty(max(E, 1), dtype=torch.float32, device=device)
         self.keep_bits = torch.empty(max(nw, 1), dtype=torch.int32, device=device)
 
-    def score(self, q, k_pages, v_pages, stream=None):
-        fork_attn_decode(q, k_pages, v_pages, self.plan, self.out, self.lse, stream)
+    def score(self, q, k_pages, v_pages=None, stream=None):
+        fork_attn_score_lse(q, k_pages, self.plan, self.lse, stream)
         fork_attn_score(q, k_pages, self.plan, self.lse, self.scores, stream)
         return self.scores
 

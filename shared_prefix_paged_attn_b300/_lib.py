@@ -83,6 +83,7 @@ SIGNATURES = {
     "fork_attn_compact_shared": (c_int32, [c_void_p, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int64)]),
     "fork_attn_merge_parts": (c_int32, [c_void_p, c_void_p, c_int32, ctypes.c_int64, c_void_p, c_int32, c_void_p,
                                          c_void_p]),
+    "fork_attn_score_lse": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
     "fork_attn_score": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
     "fork_attn_topk": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
     "fork_attn_score_sizes": (c_int32, [c_void_p, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int64)]),

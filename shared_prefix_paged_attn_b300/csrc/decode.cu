@@ -29,7 +29,9 @@ int set_smem_attr() {
     if (!done[dev]) {
         if (cudaFuncSetAttribute(fa::rowk::row_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  int(fa::rowk::kSmemBytes)) != cudaSuccess ||
-            cudaFuncSetAttribute(fa::tck::tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            cudaFuncSetAttribute(fa::tck::tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(fa::tck::kSmemBytes)) != cudaSuccess ||
+            cudaFuncSetAttribute(fa::tck::tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  int(fa::tck::kSmemBytes)) != cudaSuccess ||
             cudaFuncSetAttribute(fa::r8k::row8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  int(fa::r8k::kSmemBytes)) != cudaSuccess)
@@ -37,10 +39,13 @@ int set_smem_attr() {
         // the tcgen05 kernel re-splits its registers with setmaxnreg; the split must fit in
         // what the block is launched with, or the increase would wait forever
         cudaFuncAttributes fattr;
-        if (cudaFuncGetAttributes(&fattr, fa::tck::tc_kernel) != cudaSuccess) return FA_ERR_CUDA;
-        if (int64_t(fattr.numRegs) * fa::tck::kThreads <
-            128 * int64_t(fa::tck::kLowRegs) + int64_t(fa::tck::kThreads - 128) * fa::tck::kHighRegs)
-            return FA_ERR_UNSUPPORTED;
+        for (const void *k : {reinterpret_cast<const void *>(fa::tck::tc_kernel<false>),
+                              reinterpret_cast<const void *>(fa::tck::tc_kernel<true>)}) {
+            if (cudaFuncGetAttributes(&fattr, k) != cudaSuccess) return FA_ERR_CUDA;
+            if (int64_t(fattr.numRegs) * fa::tck::kThreads <
+                128 * int64_t(fa::tck::kLowRegs) + int64_t(fa::tck::kThreads - 128) * fa::tck::kHighRegs)
+                return FA_ERR_UNSUPPORTED;
+        }
         done[dev] = true;
     }
     return FA_OK;
@@ -123,7 +128,9 @@ int launch_all(const fa::DecodeParams &p, const fa_plan *plan, cudaStream_t st, 
     };
     bool ok = true;
     if (chain) {
-        if (p.n_items_tc > 0) ok = ok && launch(fa::tck::tc_kernel, p.tc_ctas, fa::tck::kThreads, fa::tck::kSmemBytes);
+        if (p.n_items_tc > 0)
+            ok = ok && (p.lse_only ? launch(fa::tck::tc_kernel<true>, p.tc_ctas, fa::tck::kThreads, fa::tck::kSmemBytes)
+                                   : launch(fa::tck::tc_kernel<false>, p.tc_ctas, fa::tck::kThreads, fa::tck::kSmemBytes));
         if (p.n_items_r8 > 0) ok = ok && launch(fa::r8k::row8_kernel, p.n_items_r8, fa::r8k::kThreads, fa::r8k::kSmemBytes);
         if (p.n_items > 0) ok = ok && launch(fa::rowk::row_kernel, p.n_items, fa::rowk::kThreads, fa::rowk::kSmemBytes);
     } else {
@@ -134,7 +141,9 @@ int launch_all(const fa::DecodeParams &p, const fa_plan *plan, cudaStream_t st, 
         if (p.n_items > 0) ok = ok && launch(fa::rowk::row_kernel, p.n_items, fa::rowk::kThreads, fa::rowk::kSmemBytes);
         rec(3);
         rec(4);
-        if (p.n_items_tc > 0) ok = ok && launch(fa::tck::tc_kernel, p.tc_ctas, fa::tck::kThreads, fa::tck::kSmemBytes);
+        if (p.n_items_tc > 0)
+            ok = ok && (p.lse_only ? launch(fa::tck::tc_kernel<true>, p.tc_ctas, fa::tck::kThreads, fa::tck::kSmemBytes)
+                                   : launch(fa::tck::tc_kernel<false>, p.tc_ctas, fa::tck::kThreads, fa::tck::kSmemBytes));
         rec(5);
     }
     rec(6);
@@ -302,4 +311,21 @@ extern "C" int fork_attn_merge_parts(const float *part_out, const float *part_ls
     fa::mergek::merge_parts_kernel<<<unsigned(blocks), fa::mergek::kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
         part_out, part_lse, n_parts, rows, out, out_dtype, lse);
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+extern "C" int fork_attn_score_lse(const void *q, const void *k_pages, const fa_plan *plan, float *lse, void *stream) {
+    if (!plan || !q || !k_pages || !lse) return FA_ERR_NULL;
+    if (!plan->representatives) return FA_ERR_INVALID;
+    if (!plan->uploaded) return FA_ERR_NOT_UPLOADED;
+    if (!aligned(q, 16) || !aligned(k_pages, 16) || !aligned(lse, 16)) return FA_ERR_ALIGN;
+    int rc = set_smem_attr();
+    if (rc != FA_OK) return rc;
+    fa::DecodeParams p;
+    // V is never read: its tensor maps are encoded over the K pages
+    rc = fill_params(plan, q, k_pages, k_pages, nullptr, lse, plan->dev_scratch, p);
+    if (rc != FA_OK) return rc;
+    if (p.n_items > 0 || p.n_items_r8 > 0) return FA_ERR_INVALID;  // representative plans run on tcgen05 only
+    p.lse_only = 1;
+    plan->err_word = p.err;
+    return launch_all(p, plan, static_cast<cudaStream_t>(stream), nullptr, true);
 }

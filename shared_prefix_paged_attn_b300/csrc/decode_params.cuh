@@ -40,6 +40,7 @@ struct DecodeParams {
     int32_t total_rows;  // total_q * Hq
     int32_t n_partial_rows;  // rows of part_o / part_lse
     int32_t n_mask_words;    // words of mask_words
+    int32_t lse_only;        // 1: only each row's lse (no V, no P V; partial O rows are zeros, out unused)
 };
 
 // Checked build (FORK_ATTN_CHECKED): every page id and row record the kernels take from the

@@ -21,7 +21,9 @@ namespace mergek {
 constexpr int kThreads = 256;
 
 __device__ __forceinline__ void store_row(const DecodeParams &p, int row, int lane, float4 acc, float lse) {
-    if (p.out_dtype == FA_F32) {
+    if (p.out == nullptr) {
+        // lse only
+    } else if (p.out_dtype == FA_F32) {
         *reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.out) + size_t(row) * kHeadDim + lane * 4) = acc;
     } else {
         uint2 pk = make_uint2(ptx::pack_bf16(acc.x, acc.y), ptx::pack_bf16(acc.z, acc.w));

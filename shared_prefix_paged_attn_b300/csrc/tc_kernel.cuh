@@ -186,7 +186,7 @@ __device__ __forceinline__ void producer(const DecodeParams &p, Smem &sm, const 
 // two sequences share no TMEM columns; the K/V stage-free barriers take one arrival per M
 // tile.  Per tile j: O_m (+)= P_m(j-1) V_(j-1), then S_m = Q_m K_j^T (S_m aliases P_m, so
 // it follows the P V that reads P_m).
-__device__ __forceinline__ void mma_issuer(Smem &sm, uint32_t tmem, int T, int m, int lane) {
+__device__ __forceinline__ void mma_issuer(Smem &sm, uint32_t tmem, int T, int m, int lane, bool lse_only) {
     const volatile int32_t *abort = &sm.abort;
     const uint32_t qa = ptx::smem_u32(sm.q);
     bool ok = true;
@@ -236,12 +236,23 @@ __device__ __forceinline__ void mma_issuer(Smem &sm, uint32_t tmem, int T, int m
         return true;
     };
     for (int j = 0; j < T; ++j) {
-        if (j > 0 && !pv(j - 1)) break;
+        if (j > 0) {
+            if (lse_only) {  // no P V: S_m is free again once the softmax has read it
+                if (!wait(sm.pfull[m], (j - 1) & 1)) break;
+            } else if (!pv(j - 1)) {
+                break;
+            }
+        }
         if (!wait(sm.kfull[j % kKStages], (j / kKStages) & 1)) break;
         tc::fence_after();
         qk(j);
     }
-    if (ok) pv(T - 1);
+    if (ok) {
+        if (lse_only)
+            wait(sm.pfull[m], (T - 1) & 1);
+        else
+            pv(T - 1);
+    }
     if (!ok && lane == 0) *reinterpret_cast<volatile int32_t *>(&sm.abort) = 1;
     // all MMAs issued by either MMA warp are complete before TMEM is reused or freed (fin
     // takes one arrival per M tile), and the last arrivals on the stage-free barriers have
@@ -254,13 +265,14 @@ __device__ __forceinline__ void mma_issuer(Smem &sm, uint32_t tmem, int T, int m
             const int jl = st + ((T - 1 - st) / kKStages) * kKStages;  // last tile on stage st
             wait_bar(ptx::smem_u32(&sm.kfree[st]), (jl / kKStages) & 1, &never);
         }
-        for (int st = 0; st < kVStages && st < T; ++st) {
+        for (int st = 0; st < kVStages && st < T && !lse_only; ++st) {
             const int jl = st + ((T - 1 - st) / kVStages) * kVStages;
             wait_bar(ptx::smem_u32(&sm.vfree[st]), (jl / kVStages) & 1, &never);
         }
     }
 }
 
+template <bool kLse>
 __device__ __forceinline__ void softmax(const DecodeParams &p, Smem &sm, const Chunk &ch, const Row &ri, bool valid, uint32_t tmem,
                         int T, int m, int wq, int lane) {
     const volatile int32_t *abort = &sm.abort;
@@ -366,7 +378,7 @@ __device__ __forceinline__ void softmax(const DecodeParams &p, Smem &sm, const C
                 pk[c] = ptx::pack_bf16(x, y);
             }
             // columns 16h .. 16h+15 held scores already in registers
-            tc::st16(tS + 16 * h, pk);
+            if (!kLse) tc::st16(tS + 16 * h, pk);
         }
         {
             float a0, a1, b0, b1, c0, c1, d0, d1;
@@ -377,7 +389,7 @@ __device__ __forceinline__ void softmax(const DecodeParams &p, Smem &sm, const C
             lrun += ((a0 + a1) + (b0 + b1)) + ((c0 + c1) + (d0 + d1));
         }
 
-        if (rescale) {
+        if (rescale && !kLse) {
             // O of the previous tiles (the P V MMA of tile j-1 must be done) times alpha
             ok = __all_sync(0xffffffffu, wait_bar(ptx::smem_u32(&sm.odone[m]), (j - 1) & 1, abort));
             if (!ok) break;
@@ -402,21 +414,28 @@ __device__ __forceinline__ void softmax(const DecodeParams &p, Smem &sm, const C
         return;
     }
 
-    // ---- epilogue: O / l, natural-log LSE ----
-    ok = __all_sync(0xffffffffu, wait_bar(ptx::smem_u32(&sm.odone[m]), (T - 1) & 1, abort));
-    if (!ok) {
-        if (lane == 0) fail(sm, p.err);
-        return;
+    // ---- epilogue: O / l, natural-log LSE (lse only: zero partial O rows, no out) ----
+    if (!kLse) {
+        ok = __all_sync(0xffffffffu, wait_bar(ptx::smem_u32(&sm.odone[m]), (T - 1) & 1, abort));
+        if (!ok) {
+            if (lane == 0) fail(sm, p.err);
+            return;
+        }
+        tc::fence_after();
     }
-    tc::fence_after();
     const float inv = lrun > 0.f ? 1.f / lrun : 0.f;
     const float lse = lrun > 0.f ? (mrun + log2f(lrun)) * 0.69314718055994531f : -INFINITY;
 #pragma unroll
     for (int h = 0; h < 4; ++h) {
         uint32_t o[32];
-        tc::ld32(tO + 32 * h, o);
-        tc::ld_wait();
-        tc::tie32(o);
+        if (!kLse) {
+            tc::ld32(tO + 32 * h, o);
+            tc::ld_wait();
+            tc::tie32(o);
+        } else {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) o[c] = 0u;
+        }
         if (!valid) continue;
         if (ri.prow >= 0) {
             float *dst = p.part_o + size_t(ri.prow) * kHeadDim + 32 * h;
@@ -425,6 +444,8 @@ __device__ __forceinline__ void softmax(const DecodeParams &p, Smem &sm, const C
                 *reinterpret_cast<float4 *>(dst + c) =
                     make_float4(__uint_as_float(o[c]) * inv, __uint_as_float(o[c + 1]) * inv,
                                 __uint_as_float(o[c + 2]) * inv, __uint_as_float(o[c + 3]) * inv);
+        } else if (p.out == nullptr) {
+            // lse only: no output rows
         } else if (p.out_dtype == FA_F32) {
             float *dst = reinterpret_cast<float *>(p.out) + size_t(ri.qrow) * kHeadDim + 32 * h;
 #pragma unroll
@@ -476,6 +497,8 @@ __device__ __forceinline__ void inval_barriers(Smem &sm) {
 // (header word 1) until none is left, so that the SMs they leave to the row kernels are
 // known and a CTA that runs out of work frees its SM at once.  The last CTA to leave resets
 // the counters (header words 1 and 2) for the next decode.
+// kLse: only each row's lse (no V, no P V; partial O rows are zeros and out is not written).
+template <bool kLse>
 __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__ DecodeParams p) {
     extern __shared__ uint8_t smem_raw[];
     Smem &sm = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -532,11 +555,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
             if (warp == 0) {
                 producer<false>(p, sm, it, ch, T, lane);
             } else if (warp == 1) {
-                mma_issuer(sm, tmem, T, 0, lane);
+                mma_issuer(sm, tmem, T, 0, lane, kLse);
             } else if (warp == 3) {
-                if (MT > 1) mma_issuer(sm, tmem, T, 1, lane);
+                if (MT > 1) mma_issuer(sm, tmem, T, 1, lane, kLse);
             } else if (warp == 2) {
-                producer<true>(p, sm, it, ch, T, lane);
+                if (!kLse) producer<true>(p, sm, it, ch, T, lane);
             }
             tc::fence_before();
             __syncthreads();  // C
@@ -590,7 +613,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
             tc::fence_before();
             __syncthreads();  // B
             tc::fence_after();
-            if (sm_m < MT) softmax(p, sm, ch, ri, valid, tmem, T, sm_m, warp & 3, lane);
+            if (sm_m < MT) softmax<kLse>(p, sm, ch, ri, valid, tmem, T, sm_m, warp & 3, lane);
             tc::fence_before();
             __syncthreads();  // C
             tc::fence_after();

@@ -164,3 +164,20 @@ def test_full_size_long_context_scoring():
         assert np.array_equal(kb, expected_keep(got, ks[b]))
     ws.q, ws.k_pages, ws.v_pages = ws.q.cpu(), ws.k_pages.cpu(), ws.v_pages.cpu()
     check_scores(ws, scores, branches=[0])
+
+
+@pytest.mark.parametrize("cfg", [2, 4, 5])
+def test_lse_pass_equals_the_decode_lse_bitwise(cfg):
+    # the lse-only pass runs the decode's kernels without V, P V or output rows: every
+    # representative row's lse carries the same bits as the full decode's
+    dev = torch.device("cuda")
+    ws = W.with_representatives(W.make(cfg, small=True), [0, 1, 2], reps=16)
+    sc = fa.KeyScorer(ws)
+    q, k, v = ws.q.to(dev), ws.k_pages.to(dev), ws.v_pages.to(dev)
+    fa.fork_attn_decode(q, k, v, sc.plan, sc.out, sc.lse)
+    ref = sc.lse.clone()
+    sc.lse.fill_(float("nan"))
+    fa.fork_attn_score_lse(q, k, sc.plan, sc.lse)
+    torch.cuda.synchronize()
+    assert fa.fork_attn_check(sc.plan) == 0
+    assert torch.equal(sc.lse, ref)
