@@ -514,7 +514,9 @@ def measure_scoring(args, dev, flush, steps):
                            "exp_per_s": keys * ws.meta["reps"] * ws.num_q_heads / (ms[1] * 1e-3)},
             "lse_pass_tflops": flops2 / (ms[0] * 1e-3) / 1e12,  # its QK^T, the same contraction as pass 2
             "keep": "a quarter of each branch's visible entries", "steps": steps,
-            "clocks": clk.record(), "gpu_launches": steps * 6}
+            "clocks": clk.record(),
+            # lse pass: the tcgen05 kernel (+ merge); score pass: score + head reduce; top-k
+            "gpu_launches": steps * (1 + int(st["merge_rows"] > 0) + 2 + 1)}
 
 
 def run_ours(args):
