@@ -64,3 +64,29 @@ def test_checked_build_exports_the_same_symbols():
     lib = ctypes.CDLL(path)
     for name in _lib.SIGNATURES:
         assert hasattr(lib, name), name
+
+
+def test_merge_parts_and_scoring_refuse_bad_arguments_before_any_launch():
+    import ctypes
+    from shared_prefix_paged_attn_b300 import _lib
+    import shared_prefix_paged_attn_b300 as fa
+    from shared_prefix_paged_attn_b300 import workloads as W
+    lib = _lib.load()
+    p = ctypes.c_void_p(1 << 20)  # never dereferenced: every call below fails its checks first
+    assert lib.fork_attn_merge_parts(None, p, 1, 4, p, fa.FA_F32, p, None) == -1
+    assert lib.fork_attn_merge_parts(p, p, 0, 4, p, fa.FA_F32, p, None) == -2
+    assert lib.fork_attn_merge_parts(p, p, 1, -1, p, fa.FA_F32, p, None) == -2
+    assert lib.fork_attn_merge_parts(p, p, 1, 4, p, 7, p, None) == -2
+    assert lib.fork_attn_merge_parts(ctypes.c_void_p((1 << 20) + 4), p, 1, 4, p, fa.FA_F32, p, None) == -5
+    assert lib.fork_attn_merge_parts(p, p, 1, 0, p, fa.FA_F32, p, None) == 0  # nothing to do
+    # scoring calls want a representatives plan, uploaded
+    w = W.make(1, values=False)
+    plan = fa.plan_for(w)
+    assert lib.fork_attn_score(p, p, plan.handle, p, p, None) == -2
+    assert lib.fork_attn_score_lse(p, p, plan.handle, p, None) == -2
+    assert lib.fork_attn_topk(plan.handle, p, p, p, None) == -2
+    reps = fa.plan_for(W.with_representatives(W.make(1), reps=4), representatives=1)
+    assert lib.fork_attn_score(p, p, reps.handle, p, p, None) == -6
+    assert lib.fork_attn_score_lse(p, p, reps.handle, p, None) == -6
+    assert lib.fork_attn_topk(reps.handle, p, p, p, None) == -6
+    assert lib.fork_attn_score(None, p, reps.handle, p, p, None) == -1
