@@ -5,10 +5,11 @@ AgentKV blog (rit.work), "–ö–∞–∫ AgentKV –≤—ã–±–∏—Ä–∞–µ—Ç –∏ –æ—Å–≤–æ–±–æ–∂–¥–∞–
 by the mean attention of the representative queries; the highest-scoring entries are kept.
 
 Tolerance of a score (derived from the arithmetic): bf16 inputs are exact on both sides; the
-device's QK^T accumulates in fp32 (relative ~1e-6 of the dot product's magnitude), its lse
-from the decode is within ~1e-5, and exp2 is the hardware approximation (~2e-7 relative); each
-term exp(s - lse) then carries a relative error of a few 1e-5 at most, and so does their mean.
-Tested: |got - ref| <= 2e-4 * ref + 1e-9.  The kept set is compared exactly with a selection
+device's QK^T accumulates in fp32 (relative ~1e-6 of the dot product's magnitude, i.e. an
+absolute error of s around 1e-5 for |s| ~ 10), its lse is within ~1e-6 of the fp64 one, and
+exp2 is the hardware approximation (~2e-7 relative); each term exp(s - lse) then carries a
+relative error of about 1e-5 at most, and so does their mean (about 4e-7 is seen).  Tested:
+|got - ref| <= 2e-5 * ref + 1e-9.  The kept set is compared exactly with a selection
 made on the device's own scores (ties to the smaller index), and with the oracle's set where
 the oracle's k-th and (k+1)-th scores are further apart than the tolerance; where they are not,
 every entry clearly above (below) the threshold must be kept (dropped).
@@ -24,7 +25,7 @@ from shared_prefix_paged_attn_b300 import workloads as W
 
 pytestmark = pytest.mark.gpu
 
-REL, ABS = 2e-4, 1e-9
+REL, ABS = 2e-5, 1e-9
 
 
 def run_scores(w, keep_k=None):
