@@ -192,10 +192,23 @@ __device__ __forceinline__ void run_pages(const DecodeParams &p, Smem &sm, const
                     }
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-                const float m_new = fmaxf(m[mt][hr], mx);
-                const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-                const float alpha = ptx::ex2(m[mt][hr] - m_use);
-                m[mt][hr] = m_new;
+                // lazy rescale: the running max only moves when the page's maximum exceeds it
+                // by more than 2^8 (P <= 256 in bf16 then); the four lanes of a row agree
+                const float m_old = m[mt][hr];
+                float m_use = m_old;
+                const bool rescale = m_old == -INFINITY || mx > m_old + 8.f;
+                if (rescale) {
+                    const float m_new = fmaxf(m_old, mx);
+                    m_use = (m_new == -INFINITY) ? 0.f : m_new;
+                    const float alpha = ptx::ex2(m_old - m_use);
+                    m[mt][hr] = m_new;
+                    l[mt][hr] *= alpha;
+#pragma unroll
+                    for (int dt = 0; dt < 16; ++dt) {
+                        o[mt][dt][2 * hr] *= alpha;
+                        o[mt][dt][2 * hr + 1] *= alpha;
+                    }
+                }
                 float rs = 0.f;
 #pragma unroll
                 for (int nt = 0; nt < 2; ++nt)
@@ -205,12 +218,7 @@ __device__ __forceinline__ void run_pages(const DecodeParams &p, Smem &sm, const
                         sc[mt][nt][2 * hr + e] = pv;
                         rs += pv;
                     }
-                l[mt][hr] = l[mt][hr] * alpha + rs;
-#pragma unroll
-                for (int dt = 0; dt < 16; ++dt) {
-                    o[mt][dt][2 * hr] *= alpha;
-                    o[mt][dt][2 * hr + 1] *= alpha;
-                }
+                l[mt][hr] += rs;
             }
             pa[mt][0] = ptx::pack_bf16(sc[mt][0][0], sc[mt][0][1]);
             pa[mt][1] = ptx::pack_bf16(sc[mt][0][2], sc[mt][0][3]);
