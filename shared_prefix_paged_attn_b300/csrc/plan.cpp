@@ -527,14 +527,20 @@ int build_plan(Input &in, const fa_plan_opts &opts, fa_plan *plan) {
             if (r8) st.unique_slots_row8 += chunk_slots[c];
             if (r32) st.unique_slots_row32 += chunk_slots[c];
         }
-        // pages each row group can see: up to its largest causal limit (a group whose rows all
-        // lie before the chunk sees nothing of it and gets no item at all)
+        // pages each row group can see: up to its largest causal limit.  A group whose rows all
+        // lie before the chunk sees nothing of it and gets no item at all -- unless a row of
+        // it writes `out` directly (its branch's only chunk, no merge to fill the row in): then
+        // one page, which every row sees nothing of (out 0, lse -inf)
         std::vector<int32_t> group_pages(groups.size());
         for (size_t gi = 0; gi < groups.size(); ++gi) {
             int32_t lim = -1;
-            for (int32_t r = groups[gi].first; r < groups[gi].first + groups[gi].second; ++r)
+            bool direct = false;
+            for (int32_t r = groups[gi].first; r < groups[gi].first + groups[gi].second; ++r) {
                 lim = std::max(lim, em.rows[r].climit);
-            group_pages[gi] = lim < 0 ? 0 : int32_t(std::min<int64_t>(ch.n_pages, int64_t(lim) / kPageSize + 1));
+                direct = direct || em.rows[r].prow0 < 0;
+            }
+            group_pages[gi] = lim < 0 ? (direct ? 1 : 0)
+                                      : int32_t(std::min<int64_t>(ch.n_pages, int64_t(lim) / kPageSize + 1));
         }
         for (int32_t h = 0; h < Hkv; ++h) {
             for (size_t gi = 0; gi < groups.size(); ++gi) {

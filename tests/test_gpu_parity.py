@@ -216,11 +216,13 @@ def test_timed_decode_matches_decode_bitwise():
         assert torch.equal(out2, base_out) and torch.equal(lse2, base_lse)
 
 
-@pytest.mark.parametrize("cfg", [4, 5])
+@pytest.mark.parametrize("cfg", [3, 4, 5, 6])
 @pytest.mark.parametrize("world", [2, 3])
 def test_sequence_split_merged_on_the_device(cfg, world):
     # the problem split by logical position into `world` parts (each decoded on this GPU
-    # with the other entries hidden), then joined by fork_attn_merge_parts
+    # with the other entries hidden), then joined by fork_attn_merge_parts; 3: mounted pages
+    # seen at different positions by different branches; 6: the packed DAG prefill, whose
+    # causal limits fall inside the ranges
     from shared_prefix_paged_attn_b300 import shard
     w = W.make(cfg, small=True)
     dev = torch.device("cuda")
