@@ -294,25 +294,33 @@ __device__ __forceinline__ void softmax(const DecodeParams &p, Smem &sm, const C
         if (!ok && lane == 0) fail(sm, p.err);
         return;
     }
+    // the reader's visibility words of tile jj (all ones without a mask or past the chunk,
+    // which the chunk-end mask then clears), fetched one tile ahead so that their latency
+    // overlaps the tile before
+    const bool has_mask = valid && ri.mask_off >= 0;
+    auto fetch = [&](int jj, uint32_t(&w4)[4]) {
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            const int wi = 4 * jj + w;
+            w4[w] = has_mask && wi < n_words ? __ldg(p.mask_words + ri.mask_off + wi) : 0xffffffffu;
+        }
+    };
+    uint32_t nxt[4];
+    fetch(0, nxt);
     for (int j = 0; j < T; ++j) {
         // visibility of the tile's 128 tokens for this row: words of the reader, chunk end,
         // causal limit; computed while the MMA runs
         const int t0 = j * kTileTok;
-        uint32_t bits[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
-        if (valid && (ri.mask_off >= 0 || t0 + kTileTok > n_tok || ri.climit < t0 + kTileTok - 1)) {
+        uint32_t bits[4] = {nxt[0], nxt[1], nxt[2], nxt[3]};
+        if (j + 1 < T) fetch(j + 1, nxt);
+        if (valid && (t0 + kTileTok > n_tok || ri.climit < t0 + kTileTok - 1)) {
 #pragma unroll
             for (int w = 0; w < 4; ++w) {
                 const int tq = t0 + 32 * w;
-                uint32_t b = 0xffffffffu;
-                if (ri.mask_off >= 0) {
-                    const int wi = tq >> 5;
-                    b = wi < n_words ? __ldg(p.mask_words + ri.mask_off + wi) : 0u;
-                }
                 const int lt = n_tok - tq;
-                if (lt < 32) b &= lt <= 0 ? 0u : ((1u << lt) - 1u);
+                if (lt < 32) bits[w] &= lt <= 0 ? 0u : ((1u << lt) - 1u);
                 const int lc = ri.climit - tq + 1;
-                if (lc < 32) b &= lc <= 0 ? 0u : ((1u << lc) - 1u);
-                bits[w] = b;
+                if (lc < 32) bits[w] &= lc <= 0 ? 0u : ((1u << lc) - 1u);
             }
         }
         ok = __all_sync(0xffffffffu, wait_bar(ptx::smem_u32(&sm.sfull[m]), j & 1, abort));
