@@ -120,6 +120,10 @@ __device__ __forceinline__ void tma_prefetch_5d(const CUtensorMap *map, int c0, 
 // Programmatic dependent launch: this CTA no longer holds back the kernel launched after it
 // with programmatic stream serialization (that kernel may start once every CTA of this grid
 // has executed this or exited).  It orders nothing in memory.
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
 __device__ __forceinline__ void launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {

@@ -15,17 +15,20 @@
 //   warps 0 and 2        TMA producers: per 128-token tile, warp 0 loads the 8 pages of K as
 //                        2 KiB boxes (64 dims x 16 tokens, 128-byte swizzle) into a 2-stage
 //                        K ring, warp 2 the 8 pages of V as whole 4 KiB page boxes into a
-//                        3-stage V ring; pages past the chunk's end are read at an
+//                        2-stage V ring; pages past the chunk's end are read at an
 //                        out-of-range page index, which the copy fills with zeros;
 //   warps 1 and 3        MMA issuers for M tile 0 and 1 (one lane issues, the warp waits
 //                        converged); warp 1 allocates the 512 TMEM columns:
-//                        O0 [0,128) O1 [128,256) S0/P0 [256,384) S1/P1 [384,512);
+//                        O0 [0,128) O1 [128,256) S0 [256,384) S1 [384,512);
 //   warps 4-7, 8-11      softmax of M tile 0 and 1 (one row per thread, TMEM lane = row):
 //                        S from TMEM, mask (visibility words, chunk end, causal limit), base-2
 //                        online softmax with a lazy rescale (the running max is only raised
 //                        when a row's maximum grows by more than 2^8, which keeps P <= 256),
-//                        P as bf16 written back over S in TMEM for the P V MMA.
-// While one softmax warpgroup works on its tile, the tensor core runs the other one's MMAs.
+//                        P as bf16 into a shared-memory buffer, the A operand of the P V MMA.
+// S and P live apart, so the next tile's S = Q K^T is issued as soon as the softmax has
+// loaded S into registers and runs during that softmax: each M tile's chain is one softmax
+// after another, the MMAs beside it.  The one P buffer serves both M tiles in turn (tile j:
+// M tile 0, then 1); a softmax writes P once the P V that read the buffer last is done.
 // The epilogue normalises O and writes the final output (single-chunk rows) or an fp32
 // partial (O, natural-log LSE) for the merge kernel.  Every wait is bounded; on expiry the
 // CTA sets the error word, drains its copies and MMAs (bounded) and frees its TMEM.
@@ -42,16 +45,17 @@ constexpr int kTileTok = kTilePages * kPageSize;   // 128 tokens per KV tile
 constexpr int kHalfBytes = kTileTok * 128;          // 64 dims of 128 tokens: 16 KiB
 constexpr int kTileBytes = 2 * kHalfBytes;          // 32 KiB per tile of K (or V)
 constexpr int kKStages = 2;
-constexpr int kVStages = 3;
+constexpr int kVStages = 2;
 constexpr int kRows = 2 * kTcRows;                  // 256 rows per work item
 constexpr int kQHalf = kRows * 128;                 // 64 dims of 256 rows: 32 KiB
+constexpr int kPHalf = kTcRows * 128;               // 64 tokens of P for 128 rows: 16 KiB
 constexpr int kThreads = 384;
 // Register split (setmaxnreg): the block launches with kLaunchRegs per thread; warpgroup 0
 // (producer, MMA, two idle warps) gives registers back, the two softmax warpgroups take
 // more.  128 * kLowRegs + 256 * kHighRegs must not exceed 384 * (launch registers), which
 // the host checks against the compiled kernel before the first launch.
 constexpr int kLaunchRegs = 168;
-constexpr int kLowRegs = 56;
+constexpr int kLowRegs = 80;
 constexpr int kHighRegs = 208;
 static_assert(128 * kLowRegs + 256 * kHighRegs <= kThreads * kLaunchRegs, "register split fits the launch");
 constexpr uint32_t kTmemCols = 512;
@@ -61,8 +65,9 @@ struct Smem {
     alignas(1024) uint8_t q[2 * kQHalf];
     alignas(1024) uint8_t k[kKStages][kTileBytes];
     alignas(1024) uint8_t v[kVStages][kTileBytes];
+    alignas(1024) uint8_t pb[2 * kPHalf];  // P of one M tile: [token half][128 rows][64 tokens], swizzled
     alignas(8) uint64_t kfull[kKStages], kfree[kKStages], vfull[kVStages], vfree[kVStages];
-    uint64_t sfull[2], pfull[2], odone[2], fin;
+    uint64_t sfull[2], sfree[2], pfull[2], odone[2], fin;
     uint32_t tmem_base;
     int32_t abort;
     int32_t item;  // the work item the CTA is on (persistent CTAs take items from a queue)
@@ -71,7 +76,7 @@ constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
 static_assert(kSmemBytes <= 232448, "fits the 227 KiB opt-in shared memory of one CTA");
 
 constexpr uint32_t kIdescQK = tc::idesc_bf16(128, 128, false, false);  // Q, K both K-major
-constexpr uint32_t kIdescPV = tc::idesc_bf16(128, 128, false, true);   // P (TMEM), V MN-major
+constexpr uint32_t kIdescPV = tc::idesc_bf16(128, 128, false, true);   // P K-major, V MN-major
 
 // Bounded wait that also gives up once another role of the CTA has aborted.
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const volatile int32_t *abort) {
@@ -126,9 +131,8 @@ __device__ __forceinline__ void load_v_tile(const CUtensorMap *map, uint32_t dst
     __syncwarp();
 }
 
-// Producer warps: warp 0 streams K tiles into a 2-stage ring, warp 2 streams V tiles into a
-// 3-stage ring (V stays alive one pipeline step longer than K), each running ahead as far as
-// its ring allows.
+// Producer warps: warp 0 streams K tiles, warp 2 V tiles, each into a 2-stage ring, running
+// ahead as far as its ring allows.
 template <bool kIsV>
 __device__ __forceinline__ void producer(const DecodeParams &p, Smem &sm, const Item &it, const Chunk &ch, int T,
                                          int lane) {
@@ -180,13 +184,16 @@ __device__ __forceinline__ void producer(const DecodeParams &p, Smem &sm, const 
         wait_bar(ptx::smem_u32(kIsV ? &sm.vfull[j % NS] : &sm.kfull[j % NS]), (j / NS) & 1, &never);
 }
 
-// MMA warps: warp 1 issues the MMAs of M tile 0, warp 3 those of M tile 1, so that one
-// warp's barrier waits and commits overlap the other's MMAs on the tensor core.  Every lane
-// waits on the barriers (the warp stays converged); lane 0 issues the MMAs and commits.  The
-// two sequences share no TMEM columns; the K/V stage-free barriers take one arrival per M
-// tile.  Per tile j: O_m (+)= P_m(j-1) V_(j-1), then S_m = Q_m K_j^T (S_m aliases P_m, so
-// it follows the P V that reads P_m).
-__device__ __forceinline__ void mma_issuer(Smem &sm, uint32_t tmem, int T, int m, int lane, bool lse_only) {
+// MMA warps: warp 1 issues every S = Q K^T, warp 3 every O (+)= P V, each for the M tiles in
+// turn, so that a Q K^T waits only for its S to be free and its K tile -- never behind a P V
+// that waits for a softmax.  Every lane waits on the barriers (the warp stays converged);
+// one elected lane issues the MMAs and commits.  Per tile j and M tile m:
+//   warp 1: once K_j has landed and the softmax has loaded S_m(j-1) (S free),
+//           S_m = Q_m K_j^T; after the M tiles, one commit releases K_j;
+//   warp 3: once V_j has landed and P_m(j) is in the shared buffer (P full),
+//           O_m (+)= P_m(j) V_j, committing O done of M tile m; after the M tiles, one
+//           commit releases V_j (lse only: no P V).
+__device__ __forceinline__ void mma_issuer(Smem &sm, uint32_t tmem, int T, int MT, bool is_pv, int lane, bool lse_only) {
     const volatile int32_t *abort = &sm.abort;
     const uint32_t qa = ptx::smem_u32(sm.q);
     bool ok = true;
@@ -199,20 +206,24 @@ __device__ __forceinline__ void mma_issuer(Smem &sm, uint32_t tmem, int T, int m
         __syncwarp();
     };
     // descriptors are warp-uniform values computed by every lane; one elected lane issues
-    const uint64_t qdesc0 = tc::sdesc_sw128(qa + m * (kQHalf / 2), 16, 1024);
-    auto pv_issue = [&](int j) {  // O_m (+)= P_m V_j, then release V_j
+    const uint64_t pdesc0 = tc::sdesc_sw128(ptx::smem_u32(sm.pb), 16, 1024);
+    auto pv = [&](int j, int m) {  // O_m (+)= P_m V_j
         const uint64_t vdesc = tc::sdesc_sw128(ptx::smem_u32(sm.v[j % kVStages]), 2048, 1024);
-        const uint32_t d = tmem + kColO + 128 * m, a = tmem + kColS + 128 * m;
+        const uint32_t d = tmem + kColO + 128 * m;
         if (tc::elect_one()) {
 #pragma unroll
-            for (int kk = 0; kk < kTilePages; ++kk)  // +4 KiB per page: (4096 >> 4) in the address field
-                tc::mma_ts(d, a + 8 * kk, vdesc + uint64_t(kk * (4096 >> 4)), kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < kTilePages; ++kk) {
+                // K step kk = page kk: tokens 16 kk .. 16 kk + 15 of P (half kk / 4, 32-byte
+                // column kk % 4); +4 KiB per page of V: (4096 >> 4) in the address field
+                const uint64_t poff = uint64_t(((kk >> 2) * kPHalf + (kk & 3) * 32) >> 4);
+                tc::mma_ss(d, pdesc0 + poff, vdesc + uint64_t(kk * (4096 >> 4)), kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+            }
             tc::commit(ptx::smem_u32(&sm.odone[m]));
-            tc::commit(ptx::smem_u32(&sm.vfree[j % kVStages]));
         }
         __syncwarp();
     };
-    auto qk = [&](int j) {  // S_m = Q_m K_j^T, then release K_j
+    auto qk = [&](int j, int m) {  // S_m = Q_m K_j^T
+        const uint64_t qdesc0 = tc::sdesc_sw128(qa + m * (kQHalf / 2), 16, 1024);
         const uint64_t kdesc = tc::sdesc_sw128(ptx::smem_u32(sm.k[j % kKStages]), 16, 1024);
         const uint32_t d = tmem + kColS + 128 * m;
         if (tc::elect_one()) {
@@ -224,57 +235,59 @@ __device__ __forceinline__ void mma_issuer(Smem &sm, uint32_t tmem, int T, int m
                 tc::mma_ss(d, qdesc0 + qoff, kdesc + koff, kIdescQK, kk > 0 ? 1u : 0u);
             }
             tc::commit(ptx::smem_u32(&sm.sfull[m]));
-            tc::commit(ptx::smem_u32(&sm.kfree[j % kKStages]));
         }
         __syncwarp();
     };
-    auto pv = [&](int j) {
-        if (!wait(sm.vfull[j % kVStages], (j / kVStages) & 1)) return false;
-        if (!wait(sm.pfull[m], j & 1)) return false;
-        tc::fence_after();
-        pv_issue(j);
-        return true;
-    };
-    for (int j = 0; j < T; ++j) {
-        if (j > 0) {
-            if (lse_only) {  // no P V: S_m is free again once the softmax has read it
-                if (!wait(sm.pfull[m], (j - 1) & 1)) break;
-            } else if (!pv(j - 1)) {
-                break;
+    for (int j = 0; j < T && ok; ++j) {
+        if (!is_pv) {
+            if (!wait(sm.kfull[j % kKStages], (j / kKStages) & 1)) break;
+            for (int m = 0; m < MT && ok; ++m) {
+                if (j > 0 && !wait(sm.sfree[m], (j - 1) & 1)) break;
+                tc::fence_after();
+                qk(j, m);
             }
+            if (ok) commit(sm.kfree[j % kKStages]);
+        } else if (!lse_only) {
+            if (!wait(sm.vfull[j % kVStages], (j / kVStages) & 1)) break;
+            for (int m = 0; m < MT && ok; ++m) {
+                if (!wait(sm.pfull[m], j & 1)) break;
+                tc::fence_after();
+                pv(j, m);
+            }
+            if (ok) commit(sm.vfree[j % kVStages]);
         }
-        if (!wait(sm.kfull[j % kKStages], (j / kKStages) & 1)) break;
-        tc::fence_after();
-        qk(j);
-    }
-    if (ok) {
-        if (lse_only)
-            wait(sm.pfull[m], (T - 1) & 1);
-        else
-            pv(T - 1);
     }
     if (!ok && lane == 0) *reinterpret_cast<volatile int32_t *>(&sm.abort) = 1;
     // all MMAs issued by either MMA warp are complete before TMEM is reused or freed (fin
-    // takes one arrival per M tile), and the last arrivals on the stage-free barriers have
+    // takes one arrival per MMA warp), and the last arrivals on the stage-free barriers have
     // landed before the barriers are re-initialised for the next item
-    commit(sm.fin);
+    if (is_pv && lse_only) {
+        if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&sm.fin));  // issued no MMA
+        __syncwarp();
+    } else {
+        commit(sm.fin);
+    }
     const volatile int32_t never = 0;
     wait_bar(ptx::smem_u32(&sm.fin), 0, &never);
-    if (ok) {
+    if (ok && !is_pv) {
         for (int st = 0; st < kKStages && st < T; ++st) {
             const int jl = st + ((T - 1 - st) / kKStages) * kKStages;  // last tile on stage st
             wait_bar(ptx::smem_u32(&sm.kfree[st]), (jl / kKStages) & 1, &never);
         }
-        for (int st = 0; st < kVStages && st < T && !lse_only; ++st) {
+    }
+    if (ok && is_pv && !lse_only) {
+        for (int st = 0; st < kVStages && st < T; ++st) {
             const int jl = st + ((T - 1 - st) / kVStages) * kVStages;
             wait_bar(ptx::smem_u32(&sm.vfree[st]), (jl / kVStages) & 1, &never);
         }
     }
 }
 
+// Softmax warpgroup of M tile m (MT M tiles in use).  Per tile: S from TMEM, then S free for
+// the next Q K^T; P into the shared buffer once the P V that read it last is done; P full.
 template <bool kLse>
 __device__ __forceinline__ void softmax(const DecodeParams &p, Smem &sm, const Chunk &ch, const Row &ri, bool valid, uint32_t tmem,
-                        int T, int m, int wq, int lane) {
+                        int T, int m, int MT, int wq, int lane) {
     const volatile int32_t *abort = &sm.abort;
     const uint32_t lane_base = uint32_t(wq * 32) << 16;
     const uint32_t tS = tmem + lane_base + kColS + 128 * m;
@@ -284,16 +297,37 @@ __device__ __forceinline__ void softmax(const DecodeParams &p, Smem &sm, const C
     const float sl2 = p.scale_log2;
     float mrun = -INFINITY, lrun = 0.f;
     bool ok = true;
+    auto wait = [&](uint64_t &bar, uint32_t parity) -> bool {
+        return __all_sync(0xffffffffu, wait_bar(ptx::smem_u32(&bar), parity, abort)) != 0;
+    };
+    // The P buffer's uses go M tile 0, M tile 1 per tile (two M tiles) or tile after tile
+    // (one); a P V commits O done of its M tile once it has read the buffer.  The use before
+    // (tile j, M tile m) is M tile 0's of tile j (m = 1), M tile 1's of tile j - 1 (m = 0), or
+    // the M tile's own of tile j - 1 -- and that use being done implies that this M tile's
+    // own P V of tile j - 1 is, which the O rescale needs.
+    auto pbuf_free = [&](int j) {
+        if (MT == 2 && m == 1) return wait(sm.odone[0], j & 1);
+        return j == 0 || wait(sm.odone[MT == 2 ? 1 : 0], (j - 1) & 1);
+    };
 
     if (!__any_sync(0xffffffffu, valid)) {
-        // a warp of padding rows only keeps the barrier protocol: its rows are never written
+        // a warp of padding rows only keeps the barrier protocol (its rows of P are stale,
+        // and its rows of O are never written); waiting for the P buffer keeps its arrival
+        // on P full from running ahead into the next tile's phase
         for (int j = 0; j < T && ok; ++j) {
-            ok = __all_sync(0xffffffffu, wait_bar(ptx::smem_u32(&sm.sfull[m]), j & 1, abort));
-            if (ok) ptx::mbar_arrive(ptx::smem_u32(&sm.pfull[m]));
+            ok = wait(sm.sfull[m], j & 1);
+            if (!ok) break;
+            ptx::mbar_arrive(ptx::smem_u32(&sm.sfree[m]));
+            if (!kLse) {
+                ok = pbuf_free(j);
+                if (ok) ptx::mbar_arrive(ptx::smem_u32(&sm.pfull[m]));
+            }
         }
         if (!ok && lane == 0) fail(sm, p.err);
         return;
     }
+    const uint32_t prow = ptx::smem_u32(sm.pb) + uint32_t(wq * 32 + lane) * 128;  // this row of P
+    const uint32_t pswz = uint32_t(lane & 7);  // row % 8: the row's 16-byte chunk swizzle
     // the reader's visibility words of tile jj (all ones without a mask or past the chunk,
     // which the chunk-end mask then clears), fetched one tile ahead so that their latency
     // overlaps the tile before
@@ -323,7 +357,7 @@ __device__ __forceinline__ void softmax(const DecodeParams &p, Smem &sm, const C
                 if (lc < 32) bits[w] &= lc <= 0 ? 0u : ((1u << lc) - 1u);
             }
         }
-        ok = __all_sync(0xffffffffu, wait_bar(ptx::smem_u32(&sm.sfull[m]), j & 1, abort));
+        ok = wait(sm.sfull[m], j & 1);
         if (!ok) break;
         tc::fence_after();
         uint32_t s[128];
@@ -336,6 +370,9 @@ __device__ __forceinline__ void softmax(const DecodeParams &p, Smem &sm, const C
         tc::tie32(s + 32);
         tc::tie32(s + 64);
         tc::tie32(s + 96);
+        // S is in registers: the next tile's Q K^T may overwrite it
+        tc::fence_before();
+        ptx::mbar_arrive(ptx::smem_u32(&sm.sfree[m]));
 
         if (__any_sync(0xffffffffu, (bits[0] & bits[1] & bits[2] & bits[3]) != 0xffffffffu)) {
 #pragma unroll
@@ -367,26 +404,20 @@ __device__ __forceinline__ void softmax(const DecodeParams &p, Smem &sm, const C
         }
         const float muse = mrun == -INFINITY ? 0.f : mrun;
 
-        // P = 2^(s * scale * log2 e - m) as bf16 pairs over the first 64 columns of S; the
-        // scale-and-subtract and the row sum run on packed fp32 pairs
+        // P = 2^(s * scale * log2 e - m) as bf16 pairs, first into registers (while the other
+        // M tile's P V reads the buffer); the scale-and-subtract and the row sum run on packed
+        // fp32 pairs
         const uint64_t sc2 = ptx::f2(sl2, sl2), nm2 = ptx::f2(-muse, -muse);
         uint64_t rs2[4] = {0ull, 0ull, 0ull, 0ull};  // four pair-chains of the row sum
+        uint32_t pk[64];
 #pragma unroll
-        for (int h = 0; h < 4; ++h) {
-            uint32_t pk[16];
-#pragma unroll
-            for (int c = 0; c < 16; ++c) {
-                float x, y;
-                ptx::f2_split(ptx::ffma2(ptx::f2(__uint_as_float(s[32 * h + 2 * c]), __uint_as_float(s[32 * h + 2 * c + 1])),
-                                         sc2, nm2),
-                              x, y);
-                x = ptx::ex2(x);
-                y = ptx::ex2(y);
-                rs2[c & 3] = ptx::fadd2(rs2[c & 3], ptx::f2(x, y));
-                pk[c] = ptx::pack_bf16(x, y);
-            }
-            // columns 16h .. 16h+15 held scores already in registers
-            if (!kLse) tc::st16(tS + 16 * h, pk);
+        for (int c = 0; c < 64; ++c) {
+            float x, y;
+            ptx::f2_split(ptx::ffma2(ptx::f2(__uint_as_float(s[2 * c]), __uint_as_float(s[2 * c + 1])), sc2, nm2), x, y);
+            x = ptx::ex2(x);
+            y = ptx::ex2(y);
+            rs2[c & 3] = ptx::fadd2(rs2[c & 3], ptx::f2(x, y));
+            pk[c] = ptx::pack_bf16(x, y);
         }
         {
             float a0, a1, b0, b1, c0, c1, d0, d1;
@@ -396,26 +427,37 @@ __device__ __forceinline__ void softmax(const DecodeParams &p, Smem &sm, const C
             ptx::f2_split(rs2[3], d0, d1);
             lrun += ((a0 + a1) + (b0 + b1)) + ((c0 + c1) + (d0 + d1));
         }
-
-        if (rescale && !kLse) {
-            // O of the previous tiles (the P V MMA of tile j-1 must be done) times alpha
-            ok = __all_sync(0xffffffffu, wait_bar(ptx::smem_u32(&sm.odone[m]), (j - 1) & 1, abort));
+        if (!kLse) {
+            // then into the buffer once the P V that read it last is done: tokens 8 c8 ..
+            // 8 c8 + 7 are 16-byte chunk c8 % 8 of the row in token half c8 / 8
+            ok = pbuf_free(j);
             if (!ok) break;
             tc::fence_after();
 #pragma unroll
-            for (int h = 0; h < 4; ++h) {
-                uint32_t o[32];
-                tc::ld32(tO + 32 * h, o);
-                tc::ld_wait();
-                tc::tie32(o);
-#pragma unroll
-                for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-                tc::st32(tO + 32 * h, o);
-            }
+            for (int c8 = 0; c8 < 16; ++c8)
+                ptx::st_shared_v4(prow + uint32_t(c8 >> 3) * kPHalf + ((uint32_t(c8 & 7) ^ pswz) << 4), pk[4 * c8],
+                                  pk[4 * c8 + 1], pk[4 * c8 + 2], pk[4 * c8 + 3]);
         }
-        tc::st_wait();
-        tc::fence_before();
-        ptx::mbar_arrive(ptx::smem_u32(&sm.pfull[m]));
+
+        if (!kLse) {
+            if (rescale) {
+                // O of the previous tiles (this M tile's P V of tile j - 1 is done) times alpha
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    uint32_t o[32];
+                    tc::ld32(tO + 32 * h, o);
+                    tc::ld_wait();
+                    tc::tie32(o);
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+                    tc::st32(tO + 32 * h, o);
+                }
+                tc::st_wait();
+            }
+            tc::fence_proxy_async_smem();  // P, written through the generic proxy, to the MMA
+            tc::fence_before();
+            ptx::mbar_arrive(ptx::smem_u32(&sm.pfull[m]));
+        }
     }
     if (!ok) {
         if (lane == 0) fail(sm, p.err);
@@ -478,21 +520,22 @@ __device__ __forceinline__ void softmax(const DecodeParams &p, Smem &sm, const C
     }
 }
 
-__device__ __forceinline__ void init_barriers(Smem &sm, int MT) {
+__device__ __forceinline__ void init_barriers(Smem &sm) {
     for (int s = 0; s < kKStages; ++s) {
         ptx::mbar_init(ptx::smem_u32(&sm.kfull[s]), 1);
-        ptx::mbar_init(ptx::smem_u32(&sm.kfree[s]), MT);  // one arrival per MMA warp
+        ptx::mbar_init(ptx::smem_u32(&sm.kfree[s]), 1);  // one commit after the M tiles' Q K^T
     }
     for (int s = 0; s < kVStages; ++s) {
         ptx::mbar_init(ptx::smem_u32(&sm.vfull[s]), 1);
-        ptx::mbar_init(ptx::smem_u32(&sm.vfree[s]), MT);
+        ptx::mbar_init(ptx::smem_u32(&sm.vfree[s]), 1);
     }
     for (int m = 0; m < 2; ++m) {
         ptx::mbar_init(ptx::smem_u32(&sm.sfull[m]), 1);
+        ptx::mbar_init(ptx::smem_u32(&sm.sfree[m]), 128);
         ptx::mbar_init(ptx::smem_u32(&sm.pfull[m]), 128);
         ptx::mbar_init(ptx::smem_u32(&sm.odone[m]), 1);
     }
-    ptx::mbar_init(ptx::smem_u32(&sm.fin), MT);
+    ptx::mbar_init(ptx::smem_u32(&sm.fin), 2);  // one arrival per MMA warp
     ptx::fence_mbar_init();
 }
 
@@ -527,12 +570,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
         }
         return i;
     };
-    auto item_mt = [&](int i) { return p.items_tc[i].n_rows > kTcRows ? 2 : 1; };
 
     if (tid == 0) {
         sm.abort = 0;
         sm.item = next_item();
-        if (sm.item < p.n_items_tc) init_barriers(sm, item_mt(sm.item));
+        if (sm.item < p.n_items_tc) init_barriers(sm);
     }
     if (warp == 1) {
         tc::tmem_alloc(ptx::smem_u32(&sm.tmem_base), kTmemCols);
@@ -563,9 +605,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
             if (warp == 0) {
                 producer<false>(p, sm, it, ch, T, lane);
             } else if (warp == 1) {
-                mma_issuer(sm, tmem, T, 0, lane, kLse);
+                mma_issuer(sm, tmem, T, MT, false, lane, kLse);
             } else if (warp == 3) {
-                if (MT > 1) mma_issuer(sm, tmem, T, 1, lane, kLse);
+                mma_issuer(sm, tmem, T, MT, true, lane, kLse);
             } else if (warp == 2) {
                 if (!kLse) producer<true>(p, sm, it, ch, T, lane);
             }
@@ -575,7 +617,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
             if (tid == 0) {
                 inval_barriers(sm);
                 sm.item = sm.abort ? p.n_items_tc : next_item();
-                if (sm.item < p.n_items_tc) init_barriers(sm, item_mt(sm.item));
+                if (sm.item < p.n_items_tc) init_barriers(sm);
             }
             __syncthreads();  // D
         }
@@ -621,7 +663,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
             tc::fence_before();
             __syncthreads();  // B
             tc::fence_after();
-            if (sm_m < MT) softmax<kLse>(p, sm, ch, ri, valid, tmem, T, sm_m, warp & 3, lane);
+            if (sm_m < MT) softmax<kLse>(p, sm, ch, ri, valid, tmem, T, sm_m, MT, warp & 3, lane);
             tc::fence_before();
             __syncthreads();  // C
             tc::fence_after();
