@@ -67,7 +67,7 @@ struct Smem {
     alignas(1024) uint8_t v[kVStages][kTileBytes];
     alignas(1024) uint8_t pb[2 * kPHalf];  // P of one M tile: [token half][128 rows][64 tokens], swizzled
     alignas(8) uint64_t kfull[kKStages], kfree[kKStages], vfull[kVStages], vfree[kVStages];
-    uint64_t sfull[2], sfree[2], pfull[2], odone[2], fin;
+    uint64_t sfull[2], sfree[2], pfull[2][2], odone[2][2], fin;  // P full / O done per token half
     uint32_t tmem_base;
     int32_t abort;
     int32_t item;  // the work item the CTA is on (persistent CTAs take items from a queue)
@@ -207,18 +207,19 @@ __device__ __forceinline__ void mma_issuer(Smem &sm, uint32_t tmem, int T, int M
     };
     // descriptors are warp-uniform values computed by every lane; one elected lane issues
     const uint64_t pdesc0 = tc::sdesc_sw128(ptx::smem_u32(sm.pb), 16, 1024);
-    auto pv = [&](int j, int m) {  // O_m (+)= P_m V_j
+    auto pv = [&](int j, int m, int h) {  // O_m (+)= P_m V_j over tokens 64 h .. 64 h + 63
         const uint64_t vdesc = tc::sdesc_sw128(ptx::smem_u32(sm.v[j % kVStages]), 2048, 1024);
         const uint32_t d = tmem + kColO + 128 * m;
         if (tc::elect_one()) {
 #pragma unroll
-            for (int kk = 0; kk < kTilePages; ++kk) {
-                // K step kk = page kk: tokens 16 kk .. 16 kk + 15 of P (half kk / 4, 32-byte
-                // column kk % 4); +4 KiB per page of V: (4096 >> 4) in the address field
-                const uint64_t poff = uint64_t(((kk >> 2) * kPHalf + (kk & 3) * 32) >> 4);
+            for (int kq = 0; kq < 4; ++kq) {
+                // K step kk = page kk: tokens 16 kk .. 16 kk + 15 of P (token half h, 32-byte
+                // column kq); +4 KiB per page of V: (4096 >> 4) in the address field
+                const int kk = 4 * h + kq;
+                const uint64_t poff = uint64_t((h * kPHalf + kq * 32) >> 4);
                 tc::mma_ss(d, pdesc0 + poff, vdesc + uint64_t(kk * (4096 >> 4)), kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
             }
-            tc::commit(ptx::smem_u32(&sm.odone[m]));
+            tc::commit(ptx::smem_u32(&sm.odone[m][h]));
         }
         __syncwarp();
     };
@@ -250,9 +251,11 @@ __device__ __forceinline__ void mma_issuer(Smem &sm, uint32_t tmem, int T, int M
         } else if (!lse_only) {
             if (!wait(sm.vfull[j % kVStages], (j / kVStages) & 1)) break;
             for (int m = 0; m < MT && ok; ++m) {
-                if (!wait(sm.pfull[m], j & 1)) break;
-                tc::fence_after();
-                pv(j, m);
+                for (int h = 0; h < 2 && ok; ++h) {
+                    if (!wait(sm.pfull[m][h], j & 1)) break;
+                    tc::fence_after();
+                    pv(j, m, h);
+                }
             }
             if (ok) commit(sm.vfree[j % kVStages]);
         }
@@ -301,13 +304,14 @@ __device__ __forceinline__ void softmax(const DecodeParams &p, Smem &sm, const C
         return __all_sync(0xffffffffu, wait_bar(ptx::smem_u32(&bar), parity, abort)) != 0;
     };
     // The P buffer's uses go M tile 0, M tile 1 per tile (two M tiles) or tile after tile
-    // (one); a P V commits O done of its M tile once it has read the buffer.  The use before
-    // (tile j, M tile m) is M tile 0's of tile j (m = 1), M tile 1's of tile j - 1 (m = 0), or
-    // the M tile's own of tile j - 1 -- and that use being done implies that this M tile's
-    // own P V of tile j - 1 is, which the O rescale needs.
-    auto pbuf_free = [&](int j) {
-        if (MT == 2 && m == 1) return wait(sm.odone[0], j & 1);
-        return j == 0 || wait(sm.odone[MT == 2 ? 1 : 0], (j - 1) & 1);
+    // (one), each in two token halves: the P V of an M tile commits O done of half h once it
+    // has read that half.  The use before (tile j, M tile m) is M tile 0's of tile j (m = 1),
+    // M tile 1's of tile j - 1 (m = 0), or the M tile's own of tile j - 1 -- and that use's
+    // second half being done implies that this M tile's own P V of tile j - 1 is, which the O
+    // rescale needs.
+    auto pbuf_free = [&](int j, int h) {
+        if (MT == 2 && m == 1) return wait(sm.odone[0][h], j & 1);
+        return j == 0 || wait(sm.odone[MT == 2 ? 1 : 0][h], (j - 1) & 1);
     };
 
     if (!__any_sync(0xffffffffu, valid)) {
@@ -318,9 +322,9 @@ __device__ __forceinline__ void softmax(const DecodeParams &p, Smem &sm, const C
             ok = wait(sm.sfull[m], j & 1);
             if (!ok) break;
             ptx::mbar_arrive(ptx::smem_u32(&sm.sfree[m]));
-            if (!kLse) {
-                ok = pbuf_free(j);
-                if (ok) ptx::mbar_arrive(ptx::smem_u32(&sm.pfull[m]));
+            for (int h = 0; h < 2 && ok && !kLse; ++h) {
+                ok = pbuf_free(j, h);
+                if (ok) ptx::mbar_arrive(ptx::smem_u32(&sm.pfull[m][h]));
             }
         }
         if (!ok && lane == 0) fail(sm, p.err);
@@ -428,20 +432,22 @@ __device__ __forceinline__ void softmax(const DecodeParams &p, Smem &sm, const C
             lrun += ((a0 + a1) + (b0 + b1)) + ((c0 + c1) + (d0 + d1));
         }
         if (!kLse) {
-            // then into the buffer once the P V that read it last is done: tokens 8 c8 ..
-            // 8 c8 + 7 are 16-byte chunk c8 % 8 of the row in token half c8 / 8
-            ok = pbuf_free(j);
+            // then into the buffer, half by half, once the P V that read that half last is
+            // done: tokens 8 c8 .. 8 c8 + 7 are 16-byte chunk c8 % 8 of the row in token half
+            // c8 / 8; a half is handed to the P V as soon as it is stored
+            ok = pbuf_free(j, 0);
             if (!ok) break;
             tc::fence_after();
 #pragma unroll
-            for (int c8 = 0; c8 < 16; ++c8)
-                ptx::st_shared_v4(prow + uint32_t(c8 >> 3) * kPHalf + ((uint32_t(c8 & 7) ^ pswz) << 4), pk[4 * c8],
-                                  pk[4 * c8 + 1], pk[4 * c8 + 2], pk[4 * c8 + 3]);
-        }
-
-        if (!kLse) {
+            for (int c8 = 0; c8 < 8; ++c8)
+                ptx::st_shared_v4(prow + ((uint32_t(c8) ^ pswz) << 4), pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2],
+                                  pk[4 * c8 + 3]);
             if (rescale) {
-                // O of the previous tiles (this M tile's P V of tile j - 1 is done) times alpha
+                // O of the previous tiles times alpha, before the P V of this tile starts; this M
+                // tile's P V of tile j - 1 is done once the second half's last use is
+                ok = pbuf_free(j, 1);
+                if (!ok) break;
+                tc::fence_after();
 #pragma unroll
                 for (int h = 0; h < 4; ++h) {
                     uint32_t o[32];
@@ -456,7 +462,17 @@ __device__ __forceinline__ void softmax(const DecodeParams &p, Smem &sm, const C
             }
             tc::fence_proxy_async_smem();  // P, written through the generic proxy, to the MMA
             tc::fence_before();
-            ptx::mbar_arrive(ptx::smem_u32(&sm.pfull[m]));
+            ptx::mbar_arrive(ptx::smem_u32(&sm.pfull[m][0]));
+            ok = pbuf_free(j, 1);
+            if (!ok) break;
+            tc::fence_after();
+#pragma unroll
+            for (int c8 = 8; c8 < 16; ++c8)
+                ptx::st_shared_v4(prow + kPHalf + ((uint32_t(c8 & 7) ^ pswz) << 4), pk[4 * c8], pk[4 * c8 + 1],
+                                  pk[4 * c8 + 2], pk[4 * c8 + 3]);
+            tc::fence_proxy_async_smem();
+            tc::fence_before();
+            ptx::mbar_arrive(ptx::smem_u32(&sm.pfull[m][1]));
         }
     }
     if (!ok) {
@@ -466,7 +482,7 @@ __device__ __forceinline__ void softmax(const DecodeParams &p, Smem &sm, const C
 
     // ---- epilogue: O / l, natural-log LSE (lse only: zero partial O rows, no out) ----
     if (!kLse) {
-        ok = __all_sync(0xffffffffu, wait_bar(ptx::smem_u32(&sm.odone[m]), (T - 1) & 1, abort));
+        ok = __all_sync(0xffffffffu, wait_bar(ptx::smem_u32(&sm.odone[m][1]), (T - 1) & 1, abort));
         if (!ok) {
             if (lane == 0) fail(sm, p.err);
             return;
@@ -532,8 +548,10 @@ __device__ __forceinline__ void init_barriers(Smem &sm) {
     for (int m = 0; m < 2; ++m) {
         ptx::mbar_init(ptx::smem_u32(&sm.sfull[m]), 1);
         ptx::mbar_init(ptx::smem_u32(&sm.sfree[m]), 128);
-        ptx::mbar_init(ptx::smem_u32(&sm.pfull[m]), 128);
-        ptx::mbar_init(ptx::smem_u32(&sm.odone[m]), 1);
+        for (int h = 0; h < 2; ++h) {
+            ptx::mbar_init(ptx::smem_u32(&sm.pfull[m][h]), 128);
+            ptx::mbar_init(ptx::smem_u32(&sm.odone[m][h]), 1);
+        }
     }
     ptx::mbar_init(ptx::smem_u32(&sm.fin), 2);  // one arrival per MMA warp
     ptx::fence_mbar_init();
