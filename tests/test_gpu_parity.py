@@ -156,6 +156,30 @@ def test_private_pages_of_one_branch_do_not_reach_another():
     assert np.array_equal(base[1][H:], got[1][H:])
 
 
+@pytest.mark.parametrize("cfg, small", [(1, False), (4, True)])
+@pytest.mark.parametrize("tmin", [1, 16, -1])
+def test_growing_scores_force_rescales(cfg, small, tmin):
+    """Keys whose scale grows page by page along each segment (1 + (i mod 96) / 3 for the
+    i-th page listed): a row's maximum rises by about 10 (base 2) per 128-token tile, past
+    the lazy rescale's 2^8 threshold, so the kernels rescale O on most tiles (the tcgen05
+    kernel before its P V halves, the row kernels in registers).  tmin 1: every run on the
+    tcgen05 kernel; 16: the shared runs there, the private ones on the row kernels; -1: every
+    run on the row kernels.  The tiny fork has row groups of <= 16 rows (one M tile), the
+    rolling-drop one of 256 (both M tiles share the P buffer).  V is halved: with a few keys
+    carrying nearly all the weight, the bf16 rounding of P (relative 2^-9; the row sum is kept
+    in fp32) shows in out as up to 2^-9 max|V|, which for N(0,1) values reaches the 1e-2
+    bound in every kernel alike; a missing or wrong rescale is off by the order of |V|."""
+    w = copy.deepcopy(W.make(cfg, small=small))
+    factor = torch.ones(w.k_pages.shape[0])
+    for i, page in enumerate(np.asarray(w.page_ids)):
+        factor[int(page)] = 1.0 + (i % 96) / 3.0
+    w.k_pages = (w.k_pages.float() * factor[:, None, None, None]).to(torch.bfloat16)
+    w.v_pages = (w.v_pages.float() * 0.5).to(torch.bfloat16)
+    ref_out, ref_lse = oracle.fork_attn(w)
+    out, lse = gpu_decode(w, fa.FA_F32, tensor_min_rows=tmin)
+    assert_parity(out, lse, ref_out, ref_lse, f"config {cfg} growing scores, tensor_min_rows {tmin}")
+
+
 @pytest.mark.parametrize("seed", range(16))
 def test_random_caches_all_on_tensor_cores(seed):
     # every run, however few readers it has, goes to the tcgen05 kernel: mid-page starts,
