@@ -150,7 +150,10 @@ int launch_all(const fa::DecodeParams &p, const fa_plan *plan, cudaStream_t st, 
     if (needs_merge(plan)) {
         const int64_t threads = int64_t(p.total_rows) * 32;
         const int blocks = int((threads + fa::mergek::kThreads - 1) / fa::mergek::kThreads);
-        fa::mergek::merge_kernel<<<blocks, fa::mergek::kThreads, 0, st>>>(p);
+        if (plan->merge_wide)
+            fa::mergek::merge_kernel<8><<<blocks, fa::mergek::kThreads, 0, st>>>(p);
+        else
+            fa::mergek::merge_kernel<4><<<blocks, fa::mergek::kThreads, 0, st>>>(p);
     }
     rec(7);
     const bool launched = ok && cudaGetLastError() == cudaSuccess;

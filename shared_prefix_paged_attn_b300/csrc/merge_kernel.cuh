@@ -9,8 +9,10 @@
 // holds the bases of up to five partials, so a row with that many loads the record, then
 // every partial's lse and O slice at once: two dependent loads in all.  Longer lists take
 // their bases from the branch's list, the lse values spread over the lanes (max and weights
-// by shuffles), four O loads in flight at a time.  The O terms are summed in the plan's
-// fixed order either way, so the result is bitwise run-to-run deterministic.
+// by shuffles), kF O loads in flight at a time: 4, or 8 for a plan of few merged rows whose
+// partials sit mostly in such rows (fewer resident warps, which such a plan does not fill
+// anyway, and a row's loads in half the rounds).  The O terms are summed in the plan's fixed order either way, so the result is
+// bitwise run-to-run deterministic and the same for both kF.
 #pragma once
 #include "decode_params.cuh"
 #include "ptx.cuh"
@@ -32,7 +34,8 @@ __device__ __forceinline__ void store_row(const DecodeParams &p, int row, int la
     if (lane == 0) p.lse[row] = lse;
 }
 
-__global__ void __launch_bounds__(kThreads, 6) merge_kernel(const __grid_constant__ DecodeParams p) {
+template <int kF>
+__global__ void __launch_bounds__(kThreads, kF > 4 ? 4 : 6) merge_kernel(const __grid_constant__ DecodeParams p) {
     const int row = int((blockIdx.x * size_t(kThreads) + threadIdx.x) >> 5);
     const int lane = threadIdx.x & 31;
     if (row >= p.total_rows) return;
@@ -111,24 +114,24 @@ __global__ void __launch_bounds__(kThreads, 6) merge_kernel(const __grid_constan
                 pr = bases[k0 + lane] + off;
                 wl = expf(p.part_lse[pr] - M);
             }
-            // the O terms in the plan's order, four loads in flight (the last group is
+            // the O terms in the plan's order, kF loads in flight (the last group is
             // predicated rather than walked one partial at a time)
-            for (int k = 0; k < kn; k += 4) {
-                float w[4];
-                int r[4];
-                float4 v[4];
+            for (int k = 0; k < kn; k += kF) {
+                float w[kF];
+                int r[kF];
+                float4 v[kF];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
+                for (int u = 0; u < kF; ++u) {
                     w[u] = __shfl_sync(0xffffffffu, wl, (k + u) & 31);
                     r[u] = __shfl_sync(0xffffffffu, pr, (k + u) & 31);
                 }
 #pragma unroll
-                for (int u = 0; u < 4; ++u)
+                for (int u = 0; u < kF; ++u)
                     v[u] = k + u < kn && w[u] != 0.f
                                ? *reinterpret_cast<const float4 *>(p.part_o + size_t(r[u]) * kHeadDim + lane * 4)
                                : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
+                for (int u = 0; u < kF; ++u) {
                     if (k + u < kn && w[u] != 0.f) {
                         L += w[u];
                         acc.x += w[u] * v[u].x; acc.y += w[u] * v[u].y;

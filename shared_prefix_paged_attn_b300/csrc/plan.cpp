@@ -459,6 +459,13 @@ int build_plan(Input &in, const fa_plan_opts &opts, fa_plan *plan) {
             if (prow > (int64_t(1) << 31) - 1) return FA_ERR_UNSUPPORTED;
         }
     }
+    // partials merged in all, and those in rows of more than kMergeInline partials (the
+    // merge kernel's long path): when those are most of them and the rows are few, the merge
+    // keeps more of a row's partial loads in flight (measured on B300: the flat-fork merge,
+    // 512 rows of 18 partials, 11.3 -> 9.9 us and the kv-DAG one, 1024 rows, 13.7 -> 12.1 us;
+    // the rolling-drop one, 4096 rows, unchanged, and the multi-tree one, 65536 rows, 69 ->
+    // 81 us for want of resident warps)
+    int64_t merged_all = 0, merged_long = 0;
     for (int32_t b = 0; b < B; ++b) {
         fa::Branch &br = em.branches[b];
         std::memset(&br, 0, sizeof br);
@@ -484,7 +491,11 @@ int build_plan(Input &in, const fa_plan_opts &opts, fa_plan *plan) {
             }
             em.q_merge.push_back(qm);
         }
-        if (occ_count[b] != 1) st.merge_rows += int64_t(br.n_q) * in.d->num_q_heads;
+        if (occ_count[b] != 1) {
+            st.merge_rows += int64_t(br.n_q) * in.d->num_q_heads;
+            merged_all += int64_t(br.n_q) * br.n_merge;
+            if (br.n_merge > fa::kMergeInline) merged_long += int64_t(br.n_q) * br.n_merge;
+        }
     }
 
     // work items: chunk x KV head x row group (row groups shared by every head); row groups
@@ -720,6 +731,7 @@ int build_plan(Input &in, const fa_plan_opts &opts, fa_plan *plan) {
     put(L.word_off, em.word_off.data(), em.word_off.size() * 4);
     plan->partial_rows = prow;
     plan->representatives = in.reps;
+    plan->merge_wide = 2 * merged_long > merged_all && st.merge_rows <= 2048;
     return FA_OK;
 }
 

@@ -15,6 +15,7 @@ struct fa_plan {
     std::vector<uint8_t> blob;    // host copy of the device plan buffer (lay.total bytes)
     int64_t partial_rows;         // fp32 partial rows (each 128 floats + 1 lse)
     bool representatives;         // a plan of representative queries (key scoring)
+    bool merge_wide;              // few merged rows, most partials in rows of more than kMergeInline
     fa_plan_stats stats;
     int32_t tc_ctas;              // persistent CTAs of the tcgen05 kernel (<= SMs)
     // set by fork_attn_plan_upload
