@@ -28,7 +28,8 @@
 // S and P live apart, so the next tile's S = Q K^T is issued as soon as the softmax has
 // loaded S into registers and runs during that softmax: each M tile's chain is one softmax
 // after another, the MMAs beside it.  The one P buffer serves both M tiles in turn (tile j:
-// M tile 0, then 1); a softmax writes P once the P V that read the buffer last is done.
+// M tile 0, then 1), in two 64-token halves: a softmax writes a half once the P V that read
+// that half last is done, and hands each half to the P V as soon as it is stored.
 // The epilogue normalises O and writes the final output (single-chunk rows) or an fp32
 // partial (O, natural-log LSE) for the merge kernel.  Every wait is bounded; on expiry the
 // CTA sets the error word, drains its copies and MMAs (bounded) and frees its TMEM.
@@ -190,9 +191,10 @@ __device__ __forceinline__ void producer(const DecodeParams &p, Smem &sm, const 
 // one elected lane issues the MMAs and commits.  Per tile j and M tile m:
 //   warp 1: once K_j has landed and the softmax has loaded S_m(j-1) (S free),
 //           S_m = Q_m K_j^T; after the M tiles, one commit releases K_j;
-//   warp 3: once V_j has landed and P_m(j) is in the shared buffer (P full),
-//           O_m (+)= P_m(j) V_j, committing O done of M tile m; after the M tiles, one
-//           commit releases V_j (lse only: no P V).
+//   warp 3: once V_j has landed and each token half of P_m(j) is in the shared buffer
+//           (P full of that half), O_m (+)= P_m(j) V_j over that half, committing O done
+//           of (M tile m, half); after the M tiles, one commit releases V_j (lse only: no
+//           P V).
 __device__ __forceinline__ void mma_issuer(Smem &sm, uint32_t tmem, int T, int MT, bool is_pv, int lane, bool lse_only) {
     const volatile int32_t *abort = &sm.abort;
     const uint32_t qa = ptx::smem_u32(sm.q);
@@ -287,7 +289,8 @@ __device__ __forceinline__ void mma_issuer(Smem &sm, uint32_t tmem, int T, int M
 }
 
 // Softmax warpgroup of M tile m (MT M tiles in use).  Per tile: S from TMEM, then S free for
-// the next Q K^T; P into the shared buffer once the P V that read it last is done; P full.
+// the next Q K^T; P into registers, then each token half into the shared buffer once the P V
+// that read that half last is done, and P full of that half.
 template <bool kLse>
 __device__ __forceinline__ void softmax(const DecodeParams &p, Smem &sm, const Chunk &ch, const Row &ri, bool valid, uint32_t tmem,
                         int T, int m, int MT, int wq, int lane) {
